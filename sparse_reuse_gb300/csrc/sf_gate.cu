@@ -1,0 +1,290 @@
+// Gate, compaction and source resolution of one folded layer, plus the row
+// kernels around the GEMMs (RMSNorm gather, final residual) and the weight
+// repacking done at context creation.
+//
+// Gate: "SpecFold" (arXiv 2610.04875v2 summary) §3.1-§3.2 and App. B — every
+// draft position is gated by the parent-child relative residual
+// rho = ||H_i[n] - H_par(i)[n]|| / ||H_par(i)[n]|| (formula as printed in the
+// onedev.kr review, "What is different"); rho <= delta folds; the main branch
+// bypasses the gate.  Compaction: App. B, recomputed indices go to a global
+// and per-branch list.  Resolution: §A.3 / App. B, a folded position follows
+// its chain to the nearest ancestor that recomputed it.
+#include "sf_internal.h"
+
+namespace sf {
+namespace {
+
+constexpr int kGateThreads = 256;
+
+// One row of the layer input in fp32, 4 features at column c4 * 4.
+template <bool kLayer0, typename TIn>
+__device__ __forceinline__ float4 layer_input4(const GateArgs& a, int row, int c4) {
+  if constexpr (kLayer0) {
+    return load4<TIn>(reinterpret_cast<const TIn*>(a.x_in) + (size_t)row * a.d + c4 * 4);
+  } else {
+    // the previous layer's last residual add: H = h + f[source slot]
+    const int s = a.rcslot_prev[row];
+    const float4 x = *reinterpret_cast<const float4*>(a.h_prev + (size_t)row * a.d + c4 * 4);
+    const float4 f = *reinterpret_cast<const float4*>(a.f_prev + (size_t)s * a.d + c4 * 4);
+    return make_float4(x.x + f.x, x.y + f.y, x.z + f.z, x.w + f.w);
+  }
+}
+
+// Exclusive scan over the block of one int per thread; returns the prefix and
+// writes the total to *total.  `tmp` holds 32 ints.
+__device__ int block_exclusive_scan(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) tmp[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int base = warp > 0 ? tmp[warp - 1] : 0;
+  *total = tmp[nw - 1];
+  return base + x - v;
+}
+
+// Compaction (stable, ascending row id) and source resolution; run by the
+// last thread block of the gate kernel once every fold flag is in memory.
+__device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot, int* tmp) {
+  const int T = a.T, L = a.L, Bp = a.tree.Bp, R = a.tree.R;
+  for (int row = threadIdx.x; row < T; row += blockDim.x) flags[row] = __ldcg(a.fold + row);
+  __syncthreads();
+  const int chunk = (T + blockDim.x - 1) / blockDim.x;
+  const int lo = min(T, (int)threadIdx.x * chunk), hi = min(T, lo + chunk);
+  int cnt = 0;
+  for (int row = lo; row < hi; ++row) cnt += flags[row] ? 0 : 1;
+  int total = 0;
+  int s = block_exclusive_scan(cnt, tmp, &total);
+  for (int row = lo; row < hi; ++row) {
+    if (!flags[row]) {
+      slot[row] = s;
+      a.rc[s] = row;
+      if (a.rc_user) a.rc_user[s] = row;
+      ++s;
+    } else {
+      slot[row] = -1;
+    }
+  }
+  __syncthreads();
+  for (int row = threadIdx.x; row < T; row += blockDim.x) {
+    const int n = row % L, rb = row / L, i = rb % Bp, r = rb / Bp;
+    int b = i, steps = 0;
+    while (flags[(r * Bp + b) * L + n]) {
+      b = a.tree.parent[r * Bp + b];
+      if (b < 0 || ++steps > Bp) {  // cannot happen for a validated tree
+        raise_error(a.err, kErrGate);
+        b = 0;
+        break;
+      }
+    }
+    const int sl = slot[(r * Bp + b) * L + n];
+    if (sl < 0) raise_error(a.err, kErrGate);
+    a.rcslot[row] = sl < 0 ? 0 : sl;
+    if (a.src_user) a.src_user[row] = b;
+  }
+  if (threadIdx.x == 0) {
+    a.meta[0] = total;
+    for (int r = 0; r < R; ++r) a.meta[1 + r] = slot[r * Bp * L];  // main row n = 0 always recomputes
+    a.meta[1 + R] = total;
+    if (a.rc_count_user) *a.rc_count_user = total;
+  }
+}
+
+template <bool kLayer0, typename TIn>
+__global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constant__ GateArgs a) {
+  __shared__ float red[32];
+  __shared__ int tmp[32];
+  __shared__ bool is_last;
+  extern __shared__ __align__(16) unsigned char dyn[];
+
+  const int row = blockIdx.x;
+  const int L = a.L, Bp = a.tree.Bp;
+  const int n = row % L, rb = row / L, i = rb % Bp, r = rb / Bp;
+  const int prow = i > 0 ? (r * Bp + a.tree.parent[r * Bp + i]) * L + n : -1;
+  const int d4 = a.d >> 2;
+
+  float diff2 = 0.f, par2 = 0.f;
+  for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+    const float4 x = layer_input4<kLayer0, TIn>(a, row, c);
+    *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
+    if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
+    if (prow >= 0) {
+      // the parent's input is recomputed from the same operands, so it is
+      // bit-identical to what the parent's block writes
+      const float4 y = layer_input4<kLayer0, TIn>(a, prow, c);
+      const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
+      diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
+      par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+    }
+  }
+  if (prow >= 0) {
+    diff2 = block_sum(diff2, red);
+    par2 = block_sum(par2, red);
+  }
+  if (threadIdx.x == 0) {
+    // rho <= delta  <=>  ||diff||^2 <= delta^2 ||parent||^2 (covers a zero parent)
+    const uint8_t f = (prow >= 0 && a.delta > 0.f && diff2 <= a.delta * a.delta * par2) ? 1 : 0;
+    a.fold[row] = f;
+    if (a.fold_user) a.fold_user[row] = f;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  uint8_t* flags = dyn;
+  int* slot = reinterpret_cast<int*>(dyn + ((a.T + 15) & ~15));
+  compact_and_resolve(a, flags, slot, tmp);
+  if (threadIdx.x == 0) *a.ticket = 0u;
+}
+
+// RMSNorm of rows rc[g] (or g when rc is null), g < count, gathered into a
+// dense [count][d] activation matrix.
+template <typename TAct>
+__global__ void __launch_bounds__(256) rmsnorm_gather_kernel(const float* X, const int32_t* rc, const int32_t* count_ptr,
+                                                             int max_rows, const float* gain, float eps, TAct* out,
+                                                             int d, unsigned* err) {
+  __shared__ float red[32];
+  const int count = count_ptr ? *count_ptr : max_rows;
+  const int d4 = d >> 2;
+  for (int g = blockIdx.x; g < count; g += gridDim.x) {
+    int row = rc ? rc[g] : g;
+    if (row < 0 || row >= max_rows) {
+      raise_error(err, kErrNorm);
+      row = 0;
+    }
+    const float* x = X + (size_t)row * d;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+      const float4 v = *reinterpret_cast<const float4*>(x + c * 4);
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = block_sum(ss, red);
+    const float rstd = rsqrtf(ss / (float)d + eps);
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+      const float4 v = *reinterpret_cast<const float4*>(x + c * 4);
+      const float4 w = *reinterpret_cast<const float4*>(gain + c * 4);
+      store4<TAct>(out + (size_t)g * d + c * 4,
+                   make_float4(v.x * rstd * w.x, v.y * rstd * w.y, v.z * rstd * w.z, v.w * rstd * w.w));
+    }
+  }
+}
+
+// Last layer's residual add for every row, cast to the output type.
+template <typename TOut>
+__global__ void __launch_bounds__(256) final_residual_kernel(const float* h, const float* f, const int32_t* rcslot,
+                                                             TOut* out, float* dbg, int T, int d, unsigned* err) {
+  const int d4 = d >> 2;
+  for (int row = blockIdx.x; row < T; row += gridDim.x) {
+    int s = rcslot[row];
+    if (s < 0 || s >= T) {
+      raise_error(err, kErrResid);
+      s = 0;
+    }
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+      const float4 x = *reinterpret_cast<const float4*>(h + (size_t)row * d + c * 4);
+      const float4 y = *reinterpret_cast<const float4*>(f + (size_t)s * d + c * 4);
+      const float4 o = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+      store4<TOut>(out + (size_t)row * d + c * 4, o);
+      if (dbg) *reinterpret_cast<float4*>(dbg + (size_t)row * d + c * 4) = o;
+    }
+  }
+}
+
+// dst[map(n)][k] = src[k][n] for src [K][N]; map(n) = row_base + n, or with
+// interleave = 1 (gate) / 2 (up): (n / 64) * 128 + (interleave - 1) * 64 + n % 64.
+template <typename T>
+__global__ void pack_transpose_kernel(const T* src, int K, int N, T* dst, int ld_dst, int row_base, int interleave) {
+  __shared__ T tile[32][33];
+  const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+  for (int y = threadIdx.y; y < 32; y += blockDim.y) {
+    const int k = k0 + y, n = n0 + threadIdx.x;
+    if (k < K && n < N) tile[y][threadIdx.x] = src[(size_t)k * N + n];
+  }
+  __syncthreads();
+  for (int y = threadIdx.y; y < 32; y += blockDim.y) {
+    const int n = n0 + y, k = k0 + threadIdx.x;
+    if (k < K && n < N) {
+      const int drow = interleave ? (n / 64) * 128 + (interleave - 1) * 64 + (n % 64) : row_base + n;
+      dst[(size_t)drow * ld_dst + k] = tile[threadIdx.x][y];
+    }
+  }
+}
+
+int grid_rows(int rows) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return rows < 8 * sms ? (rows > 0 ? rows : 1) : 8 * sms;
+}
+
+}  // namespace
+
+cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16) {
+  const size_t dyn = ((a.T + 15) & ~15) + (size_t)a.T * sizeof(int);
+  lc.before(SF_K_GATE);
+  if (a.x_in == nullptr)
+    gate_kernel<false, float><<<a.T, kGateThreads, dyn, lc.st>>>(a);
+  else if (in_bf16)
+    gate_kernel<true, __nv_bfloat16><<<a.T, kGateThreads, dyn, lc.st>>>(a);
+  else
+    gate_kernel<true, float><<<a.T, kGateThreads, dyn, lc.st>>>(a);
+  lc.after(SF_K_GATE);
+  return lc.err;
+}
+
+cudaError_t launch_rmsnorm_gather(Launch& lc, int fam, const float* X, const int32_t* rc, const int32_t* count,
+                                  int max_rows, const float* gain, float eps, void* out, int d, int act_bf16,
+                                  unsigned* err) {
+  lc.before(fam);
+  const int grid = grid_rows(max_rows);
+  if (act_bf16)
+    rmsnorm_gather_kernel<__nv_bfloat16><<<grid, 256, 0, lc.st>>>(X, rc, count, max_rows, gain, eps,
+                                                                   (__nv_bfloat16*)out, d, err);
+  else
+    rmsnorm_gather_kernel<float><<<grid, 256, 0, lc.st>>>(X, rc, count, max_rows, gain, eps, (float*)out, d, err);
+  lc.after(fam);
+  return lc.err;
+}
+
+cudaError_t launch_final_residual(Launch& lc, const float* h, const float* f, const int32_t* rcslot, void* out,
+                                  int out_bf16, float* dbg, int T, int d, unsigned* err) {
+  lc.before(SF_K_RESIDUAL);
+  const int grid = grid_rows(T);
+  if (out_bf16)
+    final_residual_kernel<__nv_bfloat16><<<grid, 256, 0, lc.st>>>(h, f, rcslot, (__nv_bfloat16*)out, dbg, T, d, err);
+  else
+    final_residual_kernel<float><<<grid, 256, 0, lc.st>>>(h, f, rcslot, (float*)out, dbg, T, d, err);
+  lc.after(SF_K_RESIDUAL);
+  return lc.err;
+}
+
+cudaError_t launch_pack_transpose(cudaStream_t st, const void* src, int K, int N, void* dst, int ld_dst, int row_base,
+                                  int interleave, int bf16) {
+  dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
+  if (bf16)
+    pack_transpose_kernel<__nv_bfloat16><<<grid, block, 0, st>>>((const __nv_bfloat16*)src, K, N,
+                                                                 (__nv_bfloat16*)dst, ld_dst, row_base, interleave);
+  else
+    pack_transpose_kernel<float><<<grid, block, 0, st>>>((const float*)src, K, N, (float*)dst, ld_dst, row_base,
+                                                         interleave);
+  return cudaGetLastError();
+}
+
+}  // namespace sf

@@ -1,0 +1,182 @@
+// Host-side internals of libspecfold: the context and the launch functions of
+// every kernel family.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <string>
+#include <vector>
+
+#include "sf_common.cuh"
+#include "specfold.h"
+
+struct sf_layer_dev {
+  void* wqkv = nullptr;  // [Mqkv_pad][d]      packed Wq^T | Wk^T | Wv^T | 0
+  void* wo = nullptr;    // [d][q_dim]         Wo^T
+  void* wgu = nullptr;   // [2*Fp][d]          tiles of 64 gate rows + 64 up rows
+  void* wd = nullptr;    // [d][Fp]            Wd^T, zero columns past F
+  float* g1 = nullptr;   // [d] attention RMSNorm gain
+  float* g2 = nullptr;   // [d] FFN RMSNorm gain
+};
+
+struct sf_graph_key {
+  const void* hidden_in = nullptr;
+  const void* prefix_k = nullptr;
+  const void* prefix_v = nullptr;
+  void* hidden_out = nullptr;
+  void* fold = nullptr;
+  void* src = nullptr;
+  void* rc_count = nullptr;
+  void* dbg_hidden = nullptr;
+  void* dbg_rc = nullptr;
+  void* stream = nullptr;
+  int R = 0, B = 0, P = 0;
+  float delta = 0.f;
+  std::vector<int> parent;
+  bool operator==(const sf_graph_key& o) const {
+    return hidden_in == o.hidden_in && prefix_k == o.prefix_k && prefix_v == o.prefix_v &&
+           hidden_out == o.hidden_out && fold == o.fold && src == o.src && rc_count == o.rc_count &&
+           dbg_hidden == o.dbg_hidden && dbg_rc == o.dbg_rc && stream == o.stream && R == o.R &&
+           B == o.B && P == o.P && delta == o.delta && parent == o.parent;
+  }
+};
+
+struct sf_ctx {
+  sf_shapes s{};
+  int device = 0;
+  int act_bytes = 4;
+  int q_dim = 0, kv_dim = 0, Mqkv = 0, Mqkv_pad = 0, Fp = 0, Mgu = 0;
+  int T_max = 0, max_pos = 0;
+  std::vector<sf_layer_dev> layers;
+
+  // workspaces (device)
+  float* H = nullptr;       // [T_max][d] layer input (fp32 residual stream)
+  float* h = nullptr;       // [T_max][d] after attention + residual
+  float* fphys = nullptr;   // [T_max][d] FFN output of the recompute rows
+  void* xn = nullptr;       // [T_max][max(d, Fp)] normalised gathered rows (act dtype)
+  void* qkv = nullptr;      // [T_max][Mqkv_pad] physical Q|K|V table of the recompute rows
+  void* attn = nullptr;     // [T_max][q_dim] attention output of every row
+  void* u = nullptr;        // [T_max][Fp] SwiGLU activations of the recompute rows
+  float* y32 = nullptr;     // [T_max][max M] fp32 GEMM accumulators (SIMT path)
+  float* part_o = nullptr;  // [max_splits][T_max][nq][hd] prefix-attention partials
+  float* part_ml = nullptr; // [max_splits][T_max][nq][2]  (running max, denominator)
+  int max_splits = 0;
+  uint8_t* fold = nullptr;  // [T_max]
+  int32_t* rc = nullptr;    // [T_max]
+  int32_t* rcslot[2] = {nullptr, nullptr};  // [T_max], ping-pong between layers
+  int32_t* meta = nullptr;  // [0] = rc count, [1 + r] = first recompute slot of request r
+  unsigned* ticket = nullptr;
+  unsigned* err_dev = nullptr;
+  unsigned* err_host = nullptr;  // pinned mirror, refreshed at the end of every pass
+  float2* rope = nullptr;   // [max_pos][hd/2] (cos, sin), computed in double on the host
+
+  float* dbg_hidden = nullptr;
+  int32_t* dbg_rc = nullptr;
+
+  sf_stats stats{};
+  bool use_graphs = true;
+  unsigned timing_mask = 0;
+  std::vector<cudaEvent_t> ev_start, ev_stop;
+  std::vector<int> ev_family;
+  size_t ev_used = 0;
+  std::string last_error;
+
+  // cached graph of the last argument set
+  bool graph_valid = false;
+  sf_graph_key graph_key;
+  cudaGraphExec_t graph_exec = nullptr;
+  uint64_t graph_nodes = 0;
+  uint64_t graph_family[SF_K_COUNT] = {};
+};
+
+namespace sf {
+
+// Bracket for every kernel launch: counts it, records timing events when the
+// family is selected, and turns a launch error into SF_ERR_CUDA.
+struct Launch {
+  sf_ctx* ctx;
+  cudaStream_t st;
+  cudaError_t err = cudaSuccess;
+  uint64_t launches = 0;
+  uint64_t family[SF_K_COUNT] = {};
+  void before(int fam);
+  void after(int fam);
+};
+
+struct GemmArgs {
+  const void* X;           // [rows][K] activations (act dtype), K contiguous
+  int ldx;
+  const void* W;           // [M][K] packed weight (act dtype), K contiguous
+  int ldw;
+  int M, K;
+  const int32_t* count;    // device row count, or nullptr to use dense_count
+  int dense_count;
+  int max_rows;            // capacity of X / outputs
+};
+
+enum EpiKind { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2, kEpiStore = 3 };
+
+struct EpiArgs {
+  // kEpiQKV
+  void* qkv = nullptr; int qkv_ld = 0; int qk_dim = 0; int qkv_M = 0; int hd = 0;
+  const int32_t* rc = nullptr; int L = 0; int P = 0; const float2* rope = nullptr;
+  // kEpiResidual
+  float* h = nullptr; const float* H = nullptr; int h_ld = 0;
+  // kEpiSwiGLU
+  void* u = nullptr; int u_ld = 0;
+  // kEpiStore
+  float* y = nullptr; int y_ld = 0;
+};
+
+struct GateArgs {
+  const void* x_in;            // layer 0: hidden_in [T][d] (dtype); else nullptr
+  const float* h_prev;         // layer > 0: previous layer's h [T][d]
+  const float* f_prev;         // layer > 0: previous layer's FFN table [T_rc][d]
+  const int32_t* rcslot_prev;  // layer > 0: previous layer's source slots [T]
+  float* H_out;                // [T][d]
+  float* dbg;                  // [T][d] or nullptr
+  uint8_t* fold;               // [T]
+  uint8_t* fold_user;          // [T] or nullptr
+  int32_t* rc;                 // [T]
+  int32_t* rcslot;             // [T]
+  int32_t* src_user;           // [T] or nullptr
+  int32_t* meta;               // [1 + R + 1]
+  int32_t* rc_count_user;      // one int or nullptr
+  int32_t* rc_user;            // [T] or nullptr
+  unsigned* ticket;
+  unsigned* err;
+  float delta;
+  int T, d, L;
+  Tree tree;
+};
+
+// sf_gate.cu
+cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16);
+cudaError_t launch_rmsnorm_gather(Launch& lc, int fam, const float* X, const int32_t* rc,
+                                  const int32_t* count, int max_rows, const float* gain, float eps,
+                                  void* out, int d, int act_bf16, unsigned* err);
+cudaError_t launch_final_residual(Launch& lc, const float* h, const float* f, const int32_t* rcslot,
+                                  void* out, int out_bf16, float* dbg, int T, int d, unsigned* err);
+cudaError_t launch_pack_transpose(cudaStream_t st, const void* src, int K, int N, void* dst, int ld_dst,
+                                  int row_base, int interleave, int bf16);
+
+// sf_gemm.cu
+cudaError_t launch_gemm(Launch& lc, int fam, int act_bf16, const GemmArgs& g, EpiKind kind,
+                        const EpiArgs& e, float* y32);
+
+// sf_attn.cu
+struct AttnArgs {
+  const void* qkv; int ld_qkv;
+  const void* pk; const void* pv;  // this layer's [R][P][nkv][hd]
+  const int32_t* meta;
+  const int32_t* rcslot;
+  float* part_o; float* part_ml;
+  void* attn; int ld_attn;
+  int R, Bp, L, P, T, nq, nkv, hd;
+  int n_splits, split_len;
+  float scale_log2;
+  unsigned* err;
+};
+cudaError_t launch_attention(Launch& lc, int act_bf16, const AttnArgs& a);
+
+}  // namespace sf

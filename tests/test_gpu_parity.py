@@ -1,0 +1,171 @@
+"""CUDA path vs the float64 oracle through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+
+import synth
+from parity import check_free_running, check_teacher_forced, rel_err_rows, run_gpu, TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from sparse_reuse_gb300 import build
+    build.build()
+
+
+def _wl(cfg, seed=0):
+    return synth.make_workload(cfg, seed, device="cuda")
+
+
+def test_tiny_free_running():
+    cfg = synth.CONFIGS["tiny"]
+    wl = _wl(cfg)
+    gpu = run_gpu(cfg, wl, cfg.delta)
+    ref, err = check_free_running(cfg, wl, gpu, cfg.delta)
+    assert gpu["fold"].any() and (~gpu["fold"][:, :, 1:]).any()
+
+
+FP32_CASES = {
+    "dense_delta0": (dict(), 0.0),
+    "no_prefix": (dict(prefix_len=0), 0.1),
+    "main_only": (dict(n_drafts=0), 0.1),
+    "three_requests": (dict(n_requests=3, n_drafts=5, tree="random"), 0.1),
+    "ragged_block_hd128": (dict(block_len=20, head_dim=128, n_q_heads=4, n_kv_heads=1, d_ffn=300), 0.1),
+    "long_block": (dict(block_len=64, n_drafts=3, tree="random"), 0.1),
+    "fold_everything_but_main": (dict(n_drafts=4, tree="random"), 1e6),
+    "siblings": (dict(n_drafts=6, tree="siblings"), 0.1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FP32_CASES))
+def test_fp32_variants_free_running(name):
+    kw, delta = FP32_CASES[name]
+    cfg = synth.CONFIGS["tiny"].with_(n_layers=2, prefix_len=37, **kw)
+    wl = _wl(cfg, seed=1)
+    gpu = run_gpu(cfg, wl, delta)
+    check_free_running(cfg, wl, gpu, delta)
+    if delta == 0.0:
+        assert not gpu["fold"].any()
+    if delta >= 1e6:
+        assert gpu["fold"][:, :, 1:].all()
+        assert gpu["rc_count"].tolist() == [cfg.n_requests * cfg.block_len] * cfg.n_layers
+
+
+def test_identical_child_reproduces_parent():
+    cfg = synth.CONFIGS["tiny"].with_(n_layers=2, n_drafts=3)
+    wl = _wl(cfg, seed=2)
+    wl.hidden[0, 3] = wl.hidden[0, 2]
+    gpu = run_gpu(cfg, wl, 0.1)
+    assert gpu["fold"][:, 0, 3].all()
+    assert np.array_equal(gpu["out"][0, 3], gpu["out"][0, 2])
+
+
+def test_graph_replay_is_bitwise_stable():
+    import sparse_reuse_gb300 as sf
+    cfg = synth.CONFIGS["tiny"].with_(n_layers=2, n_drafts=4, tree="random")
+    wl = _wl(cfg, seed=3)
+    ctx = sf.from_config(cfg, wl.weights)
+    a = run_gpu(cfg, wl, 0.1, ctx=ctx, graphs=False, debug=False)
+    b = run_gpu(cfg, wl, 0.1, ctx=ctx, graphs=True, debug=False)
+    c = run_gpu(cfg, wl, 0.1, ctx=ctx, graphs=True, debug=False)
+    st = ctx.stats()
+    ctx.close()
+    assert st["graph_replays"] >= 2
+    for k in ("out", "fold", "src", "rc_count"):
+        assert np.array_equal(a[k], b[k]) and np.array_equal(b[k], c[k])
+
+
+def test_bf16_small_free_running_dense_and_folded():
+    cfg = synth.small_config(n_layers=3, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=128, d_ffn=512,
+                             dtype="bf16", block_len=32, prefix_len=96, n_drafts=4)
+    wl = _wl(cfg, seed=4)
+    for delta in (0.0, 0.1):
+        gpu = run_gpu(cfg, wl, delta)
+        check_teacher_forced(cfg, wl, gpu, delta, range(cfg.n_layers))
+        if delta == 0.0:
+            check_free_running(cfg, wl, gpu, delta)
+
+
+def test_1p5b_all_layers_teacher_forced():
+    cfg = synth.CONFIGS["1.5b"]
+    wl = _wl(cfg)
+    gpu = run_gpu(cfg, wl, cfg.delta)
+    worst = check_teacher_forced(cfg, wl, gpu, cfg.delta, range(cfg.n_layers))
+    assert worst <= TOL["bf16"]
+
+
+def test_1p5b_dense_free_running():
+    cfg = synth.CONFIGS["1.5b"]
+    wl = _wl(cfg)
+    gpu = run_gpu(cfg, wl, 0.0, debug=False)
+    assert not gpu["fold"].any()
+    check_free_running(cfg, wl, gpu, 0.0)
+
+
+@pytest.mark.parametrize("name,delta", [("7b", 0.1), ("7b", 0.0)] +
+                         [("8b", d) for d in synth.DELTA_SWEEP_8B])
+def test_large_configs_sampled_layers(name, delta):
+    cfg = synth.CONFIGS[name]
+    wl = _wl(cfg)
+    gpu = run_gpu(cfg, wl, delta)
+    check_teacher_forced(cfg, wl, gpu, delta, [0, cfg.n_layers // 2, cfg.n_layers - 1])
+
+
+@pytest.mark.parametrize("B", synth.DRAFT_SWEEP_14B)
+def test_14b_batched_draft_sweep_sampled_layers(B):
+    cfg = synth.CONFIGS["14b"].with_(n_drafts=B)
+    wl = _wl(cfg)
+    gpu = run_gpu(cfg, wl, cfg.delta)
+    check_teacher_forced(cfg, wl, gpu, cfg.delta, [0, cfg.n_layers - 1])
+
+
+# ------------------------------------------------------------------ error paths
+
+def test_argument_and_tree_errors_launch_nothing():
+    import torch
+    import sparse_reuse_gb300 as sf
+    cfg = synth.CONFIGS["tiny"]
+    wl = _wl(cfg)
+    ctx = sf.from_config(cfg, wl.weights)
+    before = ctx.stats()["kernel_launches"]
+    bad = [
+        (dict(parent=np.array([[0, 0, 1]])), sf.SF_ERR_TREE),
+        (dict(parent=np.array([[-1, 1, 1]])), sf.SF_ERR_TREE),
+        (dict(parent=np.array([[-1, 0, 3]])), sf.SF_ERR_TREE),
+        (dict(delta=-0.1), sf.SF_ERR_INVALID_ARG),
+        (dict(delta=float("nan")), sf.SF_ERR_INVALID_ARG),
+        (dict(delta=float("inf")), sf.SF_ERR_INVALID_ARG),
+        (dict(parent=np.array([[-1, 0, 1, 2]])), sf.SF_ERR_SHAPE),
+        (dict(P=cfg.prefix_len + 1), sf.SF_ERR_SHAPE),
+        (dict(hidden=0), sf.SF_ERR_INVALID_ARG),
+    ]
+    out = torch.empty_like(wl.hidden)
+    for kw, status in bad:
+        parent = kw.get("parent", wl.parents)
+        with pytest.raises(sf.SpecFoldError) as ei:
+            sf.sf_verify(ctx.ctx, None, kw.get("hidden", wl.hidden.data_ptr()), parent, wl.prefix_k.data_ptr(),
+                         wl.prefix_v.data_ptr(), parent.shape[0], parent.shape[1] - 1, kw.get("P", cfg.prefix_len),
+                         kw.get("delta", 0.1), out.data_ptr())
+        assert ei.value.status == status, (kw, ei.value)
+    assert ctx.stats()["kernel_launches"] == before
+    # R = 0 is an empty pass
+    sf.sf_verify(ctx.ctx, None, wl.hidden.data_ptr(), np.zeros((0, 3), np.int32), None, None, 0, 2, 0, 0.1,
+                 out.data_ptr())
+    assert ctx.stats()["kernel_launches"] == before
+    ctx.close()
+
+
+def test_timing_hooks_report_every_family():
+    import sparse_reuse_gb300 as sf
+    cfg = synth.CONFIGS["tiny"]
+    wl = _wl(cfg)
+    ctx = sf.from_config(cfg, wl.weights)
+    sf.sf_timing_begin(ctx.ctx, sf.FAMILIES)
+    ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, 0.1)
+    t = sf.sf_timing_read(ctx.ctx)
+    sf.sf_timing_begin(ctx.ctx, [])
+    ctx.close()
+    for fam in ("gate", "norm", "gemm_qkv", "attn_prefix", "attn_block", "gemm_o", "gemm_gateup",
+                "gemm_down", "residual"):
+        assert fam in t and t[fam][0] > 0 and t[fam][1] >= 1
