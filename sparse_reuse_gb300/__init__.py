@@ -1,8 +1,8 @@
 """Python binding of libspecfold (the C ABI in include/specfold.h).
 
 Argument marshalling only: every step of the verification pass runs in the
-library's CUDA kernels.  Importing this package loads the in-tree
-libspecfold.so; if it is missing the import fails (build it with
+library's CUDA kernels.  The in-tree libspecfold.so is loaded on the first
+call into the binding; if it is missing that call raises ImportError (build it with
 ``python -c "import __graft_entry__ as g; g.build()"`` or
 ``python sparse_reuse_gb300/build.py``).  PyTorch provides device memory and
 streams only.
@@ -79,7 +79,20 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-lib = _load()
+class _LazyLib:
+    """Loads libspecfold.so on first use so that the build module inside this
+    package can be imported on a machine where it is not built yet; any call
+    into the binding without the library raises ImportError."""
+
+    _cdll = None
+
+    def __getattr__(self, name):
+        if _LazyLib._cdll is None:
+            _LazyLib._cdll = _load()
+        return getattr(_LazyLib._cdll, name)
+
+
+lib = _LazyLib()
 
 
 def _check(st: int, ctx=None, what: str = ""):
