@@ -41,7 +41,7 @@ FP32_CASES = {
 @pytest.mark.parametrize("name", sorted(FP32_CASES))
 def test_fp32_variants_free_running(name):
     kw, delta = FP32_CASES[name]
-    cfg = synth.CONFIGS["tiny"].with_(n_layers=2, prefix_len=37, **kw)
+    cfg = synth.CONFIGS["tiny"].with_(**dict(dict(n_layers=2, prefix_len=37), **kw))
     wl = _wl(cfg, seed=1)
     gpu = run_gpu(cfg, wl, delta)
     check_free_running(cfg, wl, gpu, delta)
@@ -62,18 +62,37 @@ def test_identical_child_reproduces_parent():
 
 
 def test_graph_replay_is_bitwise_stable():
+    import torch
     import sparse_reuse_gb300 as sf
     cfg = synth.CONFIGS["tiny"].with_(n_layers=2, n_drafts=4, tree="random")
     wl = _wl(cfg, seed=3)
     ctx = sf.from_config(cfg, wl.weights)
-    a = run_gpu(cfg, wl, 0.1, ctx=ctx, graphs=False, debug=False)
-    b = run_gpu(cfg, wl, 0.1, ctx=ctx, graphs=True, debug=False)
-    c = run_gpu(cfg, wl, 0.1, ctx=ctx, graphs=True, debug=False)
+    stream = torch.cuda.Stream()
+    out = torch.empty_like(wl.hidden)
+    fold = torch.empty((cfg.n_layers, 1, cfg.n_branches, cfg.block_len), dtype=torch.uint8, device="cuda")
+    src = torch.empty(fold.shape, dtype=torch.int32, device="cuda")
+    rcc = torch.empty((cfg.n_layers,), dtype=torch.int32, device="cuda")
+    res = []
+    for graphs in (False, True, True, True):
+        ctx.set_graphs(graphs)
+        ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, 0.1, out=out, fold=fold, src=src,
+                   rc_count=rcc, stream=stream)
+        ctx.sync(stream)
+        res.append([t.clone() for t in (out, fold, src, rcc)])
     st = ctx.stats()
+    # a different tree recaptures and gives a different result
+    p2 = wl.parents.copy()
+    p2[0, -1] = 0
+    ctx.verify(wl.hidden, p2, wl.prefix_k, wl.prefix_v, 0.1, out=out, fold=fold, src=src, rc_count=rcc,
+               stream=stream)
+    ctx.sync(stream)
+    st2 = ctx.stats()
     ctx.close()
-    assert st["graph_replays"] >= 2
-    for k in ("out", "fold", "src", "rc_count"):
-        assert np.array_equal(a[k], b[k]) and np.array_equal(b[k], c[k])
+    assert st["graph_replays"] == 3 and st2["graph_replays"] == 4
+    for r in res[1:]:
+        for a, b in zip(res[0], r):
+            assert torch.equal(a, b)
+    assert st2["kernel_launches"] - st["kernel_launches"] == st["kernel_launches"] // 4
 
 
 def test_bf16_small_free_running_dense_and_folded():
