@@ -57,7 +57,8 @@ void free_ctx(sf_ctx* c) {
   for (auto& L : c->layers) {
     cudaFree(L.wqkv); cudaFree(L.wo); cudaFree(L.wgu); cudaFree(L.wd); cudaFree(L.g1); cudaFree(L.g2);
   }
-  void* bufs[] = {c->H, c->h, c->fphys, c->xn, c->qkv, c->attn, c->u, c->y32, c->part_o, c->part_ml,
+  void* bufs[] = {c->H, c->h, c->fphys, c->xn, c->qkv, c->attn, c->u, c->y32, c->gemm_ws, c->tile_ctr,
+                  c->part_o, c->part_ml,
                   c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->err_dev, c->rope};
   for (void* b : bufs) cudaFree(b);
   if (c->err_host) cudaFreeHost(c->err_host);
@@ -74,7 +75,7 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 namespace sf {
 
 void Launch::before(int fam) {
-  if (ctx->timing_mask & (1u << fam)) {
+  if (ctx && ctx->timing_mask & (1u << fam)) {
     if (ctx->ev_used == ctx->ev_start.size()) {
       cudaEvent_t a, b;
       cudaEventCreate(&a);
@@ -93,7 +94,7 @@ void Launch::after(int fam) {
   if (e != cudaSuccess && err == cudaSuccess) err = e;
   ++launches;
   ++family[fam];
-  if (ctx->timing_mask & (1u << fam)) {
+  if (ctx && ctx->timing_mask & (1u << fam)) {
     cudaEventRecord(ctx->ev_stop[ctx->ev_used], st);
     ++ctx->ev_used;
   }
@@ -115,6 +116,27 @@ struct PassArgs {
   int32_t* rc_count;
   const int32_t* parent;
 };
+
+// One GEMM of the layer: tcgen05 kernel for BF16 contexts, CUDA-core fp32
+// kernel for FP32 contexts.
+cudaError_t run_gemm(sf_ctx* c, Launch& lc, int fam, const GemmArgs& g, const CUtensorMap* tmA,
+                     const CUtensorMap* tmB, EpiKind kind, const EpiArgs& e) {
+  if (c->s.dtype != SF_BF16) return launch_gemm(lc, fam, 0, g, kind, e, c->y32);
+  TcGemm t{};
+  t.tmA = tmA;
+  t.tmB = tmB;
+  t.M = g.M;
+  t.K = g.K;
+  t.count = g.count;
+  t.dense_count = g.dense_count;
+  t.max_rows = g.max_rows;
+  const int n_tiles = g.count ? 1 : (g.dense_count + 255) / 256;
+  t.splits = gemm_tc_splits(g.M, g.K, n_tiles, c->gemm_ws_floats, g.max_rows);
+  t.ws = c->gemm_ws;
+  t.tile_ctr = c->tile_ctr;
+  t.err = c->err_dev;
+  return launch_gemm_tc(lc, fam, t, kind, e);
+}
 
 cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
   const sf_shapes& s = c->s;
@@ -165,7 +187,7 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     g.count = c->meta; g.dense_count = T; g.max_rows = T;
     e.qkv = c->qkv; e.qkv_ld = c->Mqkv_pad; e.qk_dim = c->q_dim + c->kv_dim; e.qkv_M = c->Mqkv;
     e.hd = s.head_dim; e.rc = c->rc; e.L = L; e.P = p.P; e.rope = c->rope;
-    if (launch_gemm(lc, SF_K_GEMM_QKV, bf16, g, kEpiQKV, e, c->y32) != cudaSuccess) return lc.err;
+    if (run_gemm(c, lc, SF_K_GEMM_QKV, g, &W.tm_wqkv, &c->tm_xn, kEpiQKV, e) != cudaSuccess) return lc.err;
 
     AttnArgs a{};
     a.qkv = c->qkv; a.ld_qkv = c->Mqkv_pad;
@@ -185,7 +207,7 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     g.X = c->attn; g.ldx = c->q_dim; g.W = W.wo; g.ldw = c->q_dim; g.M = d; g.K = c->q_dim;
     g.count = nullptr; g.dense_count = T; g.max_rows = T;
     e.h = c->h; e.H = c->H; e.h_ld = d;
-    if (launch_gemm(lc, SF_K_GEMM_O, bf16, g, kEpiResidual, e, c->y32) != cudaSuccess) return lc.err;
+    if (run_gemm(c, lc, SF_K_GEMM_O, g, &W.tm_wo, &c->tm_attn, kEpiResidual, e) != cudaSuccess) return lc.err;
 
     launch_rmsnorm_gather(lc, SF_K_NORM, c->h, c->rc, c->meta, T, W.g2, s.rms_eps, c->xn, d, bf16, c->err_dev);
 
@@ -194,14 +216,14 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     g.X = c->xn; g.ldx = d; g.W = W.wgu; g.ldw = d; g.M = c->Mgu; g.K = d;
     g.count = c->meta; g.dense_count = T; g.max_rows = T;
     e.u = c->u; e.u_ld = c->Fp;
-    if (launch_gemm(lc, SF_K_GEMM_GATEUP, bf16, g, kEpiSwiGLU, e, c->y32) != cudaSuccess) return lc.err;
+    if (run_gemm(c, lc, SF_K_GEMM_GATEUP, g, &W.tm_wgu, &c->tm_xn, kEpiSwiGLU, e) != cudaSuccess) return lc.err;
 
     g = GemmArgs{};
     e = EpiArgs{};
     g.X = c->u; g.ldx = c->Fp; g.W = W.wd; g.ldw = c->Fp; g.M = d; g.K = c->Fp;
     g.count = c->meta; g.dense_count = T; g.max_rows = T;
     e.y = c->fphys; e.y_ld = d;
-    if (launch_gemm(lc, SF_K_GEMM_DOWN, bf16, g, kEpiStore, e, c->y32) != cudaSuccess) return lc.err;
+    if (run_gemm(c, lc, SF_K_GEMM_DOWN, g, &W.tm_wd, &c->tm_u, kEpiStore, e) != cudaSuccess) return lc.err;
   }
   launch_final_residual(lc, c->h, c->fphys, c->rcslot[(nl - 1) & 1], p.hidden_out, bf16,
                         c->dbg_hidden ? c->dbg_hidden + (size_t)nl * T * d : nullptr, T, d, c->err_dev);
@@ -275,11 +297,24 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
   SF_TRY(dalloc(&c->H, (size_t)T * d * 4));
   SF_TRY(dalloc(&c->h, (size_t)T * d * 4));
   SF_TRY(dalloc(&c->fphys, (size_t)T * d * 4));
-  SF_TRY(dalloc(&c->xn, (size_t)T * std::max(d, c->Fp) * ab));
+  c->rows_cap = round_up(T, 256);
+  const int RC = c->rows_cap;
+  SF_TRY(dalloc(&c->xn, (size_t)RC * d * ab));
   SF_TRY(dalloc(&c->qkv, (size_t)T * c->Mqkv_pad * ab));
-  SF_TRY(dalloc(&c->attn, (size_t)T * c->q_dim * ab));
-  SF_TRY(dalloc(&c->u, (size_t)T * c->Fp * ab));
-  SF_TRY(dalloc(&c->y32, (size_t)T * maxM * 4));
+  SF_TRY(dalloc(&c->attn, (size_t)RC * c->q_dim * ab));
+  SF_TRY(dalloc(&c->u, (size_t)RC * c->Fp * ab));
+  if (bf16) {
+    c->gemm_ws_floats = (size_t)8 * T * std::max(c->Mqkv_pad, d);
+    SF_TRY(dalloc(&c->gemm_ws, c->gemm_ws_floats * 4));
+    SF_TRY(dalloc(&c->tile_ctr, (size_t)(maxM / 128) * (RC / 256) * sizeof(unsigned)));
+    if (!make_tmap_bf16(&c->tm_xn, c->xn, d, RC, 64) || !make_tmap_bf16(&c->tm_attn, c->attn, c->q_dim, RC, 64) ||
+        !make_tmap_bf16(&c->tm_u, c->u, c->Fp, RC, 64)) {
+      free_ctx(c);
+      return SF_ERR_CUDA;
+    }
+  } else {
+    SF_TRY(dalloc(&c->y32, (size_t)T * maxM * 4));
+  }
   SF_TRY(dalloc(&c->part_o, (size_t)c->max_splits * T * c->q_dim * 4));
   SF_TRY(dalloc(&c->part_ml, (size_t)c->max_splits * T * s.n_q_heads * 2 * 4));
   SF_TRY(dalloc(&c->fold, (size_t)T));
@@ -319,6 +354,12 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
     SF_TRY(launch_pack_transpose(0, w.w_gate, d, s.d_ffn, D.wgu, d, 0, 1, bf16));
     SF_TRY(launch_pack_transpose(0, w.w_up, d, s.d_ffn, D.wgu, d, 0, 2, bf16));
     SF_TRY(launch_pack_transpose(0, w.w_down, s.d_ffn, d, D.wd, c->Fp, 0, 0, bf16));
+    if (bf16 && (!make_tmap_bf16(&D.tm_wqkv, D.wqkv, d, c->Mqkv_pad, 128) ||
+                 !make_tmap_bf16(&D.tm_wo, D.wo, c->q_dim, d, 128) ||
+                 !make_tmap_bf16(&D.tm_wgu, D.wgu, d, c->Mgu, 128) || !make_tmap_bf16(&D.tm_wd, D.wd, c->Fp, d, 128))) {
+      free_ctx(c);
+      return SF_ERR_CUDA;
+    }
     SF_TRY(cudaMemcpy(D.g1, w.attn_norm, (size_t)d * 4, cudaMemcpyDeviceToDevice));
     SF_TRY(cudaMemcpy(D.g2, w.ffn_norm, (size_t)d * 4, cudaMemcpyDeviceToDevice));
   }

@@ -9,7 +9,6 @@
 
 namespace sf {
 
-cudaError_t launch_gemm_tc(Launch& lc, int fam, const GemmArgs& g, EpiKind kind, const EpiArgs& e);
 
 namespace {
 

@@ -2,6 +2,7 @@
 // every kernel family.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <string>
@@ -17,6 +18,8 @@ struct sf_layer_dev {
   void* wd = nullptr;    // [d][Fp]            Wd^T, zero columns past F
   float* g1 = nullptr;   // [d] attention RMSNorm gain
   float* g2 = nullptr;   // [d] FFN RMSNorm gain
+  // TMA descriptors of the packed weights (BF16 contexts)
+  alignas(64) CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd;
 };
 
 struct sf_graph_key {
@@ -57,7 +60,12 @@ struct sf_ctx {
   void* qkv = nullptr;      // [T_max][Mqkv_pad] physical Q|K|V table of the recompute rows
   void* attn = nullptr;     // [T_max][q_dim] attention output of every row
   void* u = nullptr;        // [T_max][Fp] SwiGLU activations of the recompute rows
-  float* y32 = nullptr;     // [T_max][max M] fp32 GEMM accumulators (SIMT path)
+  float* y32 = nullptr;     // [T_max][max M] fp32 GEMM accumulators (FP32 contexts)
+  int rows_cap = 0;         // activation buffers' row capacity (T_max rounded to 256)
+  float* gemm_ws = nullptr; // split-K partial sums of the tcgen05 GEMM
+  size_t gemm_ws_floats = 0;
+  unsigned* tile_ctr = nullptr;  // split-K arrival tickets
+  alignas(64) CUtensorMap tm_xn, tm_attn, tm_u;  // activation operands (BF16 contexts)
   float* part_o = nullptr;  // [max_splits][T_max][nq][hd] prefix-attention partials
   float* part_ml = nullptr; // [max_splits][T_max][nq][2]  (running max, denominator)
   int max_splits = 0;
@@ -160,7 +168,24 @@ cudaError_t launch_final_residual(Launch& lc, const float* h, const float* f, co
 cudaError_t launch_pack_transpose(cudaStream_t st, const void* src, int K, int N, void* dst, int ld_dst,
                                   int row_base, int interleave, int bf16);
 
-// sf_gemm.cu
+// sf_gemm_tc.cu (BF16 contexts)
+struct TcGemm {
+  const CUtensorMap* tmA;  // weight [M][K]
+  const CUtensorMap* tmB;  // activations [rows][K]
+  int M, K;
+  const int32_t* count;
+  int dense_count;
+  int max_rows;
+  int splits;
+  float* ws;
+  unsigned* tile_ctr;
+  unsigned* err;
+};
+bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+int gemm_tc_splits(int M, int K, int n_tiles, size_t ws_floats, int max_rows);
+cudaError_t launch_gemm_tc(Launch& lc, int fam, const TcGemm& g, EpiKind kind, const EpiArgs& e);
+
+// sf_gemm.cu (FP32 contexts)
 cudaError_t launch_gemm(Launch& lc, int fam, int act_bf16, const GemmArgs& g, EpiKind kind,
                         const EpiArgs& e, float* y32);
 

@@ -1,0 +1,76 @@
+"""The tcgen05 row-gathered GEMM against a float64 matmul of the same bf16
+operands (needs a GB300): live row counts around the 16-row MMA step, the
+64-row TMA box and the 256-row tile, K splits, and the count read on the
+device."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sf():
+    from sparse_reuse_gb300 import build
+    build.build()
+    import sparse_reuse_gb300 as m
+    return m
+
+
+def _run(sf, M, K, rows_cap, count, splits, on_device=True, seed=0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    X = (torch.randn((rows_cap, K), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    W = (torch.randn((M, K), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    Y = torch.full((rows_cap, M), float("nan"), device="cuda")
+    cnt = torch.tensor([count], dtype=torch.int32, device="cuda")
+    n_tiles = (rows_cap + 255) // 256
+    ws = torch.zeros((splits, rows_cap, M), device="cuda") if splits > 1 else None
+    ctr = torch.zeros((n_tiles * (M // 128),), dtype=torch.int32, device="cuda") if splits > 1 else None
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    p = lambda t: None if t is None else t.data_ptr()
+    sf.sfk_gemm_bf16(None, X.data_ptr(), rows_cap, W.data_ptr(), M, K, cnt.data_ptr() if on_device else None,
+                     count, Y.data_ptr(), M, splits, p(ws), p(ctr), err.data_ptr())
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    if ctr is not None:
+        assert int(ctr.abs().sum().item()) == 0     # tickets are left at zero
+    ref = X[:count].double().cpu().numpy() @ W.double().cpu().numpy().T
+    got = Y[:count].double().cpu().numpy()
+    scale = np.abs(X[:count].double().cpu().numpy()) @ np.abs(W.double().cpu().numpy().T) + 1e-30
+    assert np.all(np.abs(got - ref) <= 1e-4 * scale + 1e-6), np.max(np.abs(got - ref) / scale)
+    assert torch.isnan(Y[count:]).all()                # rows past the count are untouched
+    return Y
+
+
+@pytest.mark.parametrize("count", [1, 15, 16, 17, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 288, 511])
+def test_counts_single_split(sf, count):
+    _run(sf, 256, 512, 512, count, 1)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7, 8])
+def test_split_k(sf, splits):
+    _run(sf, 384, 1536, 300, 288, splits)
+    _run(sf, 384, 1536, 300, 50, splits, seed=1)
+
+
+def test_zero_rows_writes_nothing(sf):
+    _run(sf, 128, 128, 64, 0, 1)
+    _run(sf, 128, 128, 64, 0, 2)
+
+
+def test_dense_count_and_long_k(sf):
+    _run(sf, 128, 8960, 64, 50, 12, on_device=False)
+    _run(sf, 1536, 1536, 288, 288, 4, on_device=False)
+
+
+def test_split_results_are_deterministic(sf):
+    a = _run(sf, 256, 2048, 288, 288, 6, seed=3)
+    b = _run(sf, 256, 2048, 288, 288, 6, seed=3)
+    assert torch.equal(a[:288], b[:288])
+
+
+def test_bad_arguments_rejected(sf):
+    with pytest.raises(sf.SpecFoldError):
+        sf.sfk_gemm_bf16(None, 16, 64, 16, 100, 64, None, 1, 16, 100, 1)      # M not a multiple of 128
+    with pytest.raises(sf.SpecFoldError):
+        sf.sfk_gemm_bf16(None, 16, 64, 16, 128, 64, None, 1, 16, 128, 2)      # split without workspace
