@@ -27,17 +27,16 @@ extern "C" {
  *   count      device int32 holding the live row count (<= rows_cap), or NULL
  *              to use dense_count.
  *   Y          device fp32 [rows_cap][ldy], ldy >= M; rows >= count untouched.
- *   splits     1 .. K/64: K is split over this many CTAs per output tile.
- *   ws         device fp32 [splits][rows_cap][M] partial sums; NULL if splits == 1.
- *   tile_ctr   device uint32 [ceil(rows_cap/256) * M/128], zero before the
- *              first call and left zero by every call; NULL if splits == 1.
+ *   splits     1..6 or 8, at most K/64: K is split over a cluster of this
+ *              many CTAs per output tile, whose partial sums are added in
+ *              cluster-rank order in shared memory (no workspace).
  *   err        device uint32 error word (bit 32 = a bounded wait gave up) or NULL.
  * Errors: SF_ERR_INVALID_ARG (null operand, bad M/K/splits/ldy, unaligned
  * pointer), SF_ERR_CUDA (descriptor encoding or launch failure).
  * Asynchronous; the buffers must stay valid until the stream reaches it. */
 sf_status sfk_gemm_bf16(void* stream, const void* X, int rows_cap, const void* W, int M, int K,
-                        const int32_t* count, int dense_count, float* Y, int ldy, int splits, float* ws,
-                        uint32_t* tile_ctr, uint32_t* err);
+                        const int32_t* count, int dense_count, float* Y, int ldy, int splits,
+                        uint32_t* err);
 
 #ifdef __cplusplus
 }

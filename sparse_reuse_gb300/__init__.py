@@ -73,7 +73,7 @@ def _load() -> ctypes.CDLL:
     lib.sf_set_graphs.argtypes = [vp, c_int]
     lib.sf_timing_begin.argtypes = [vp, ctypes.c_uint]
     lib.sf_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
-    lib.sfk_gemm_bf16.argtypes = [vp, vp, c_int, vp, c_int, c_int, vp, c_int, vp, c_int, c_int, vp, vp, vp]
+    lib.sfk_gemm_bf16.argtypes = [vp, vp, c_int, vp, c_int, c_int, vp, c_int, vp, c_int, c_int, vp]
     for name in EXPORTS:
         fn = getattr(lib, name)
         if name not in ("sf_status_str", "sf_last_error"):
@@ -173,10 +173,9 @@ def sf_timing_read(ctx) -> dict:
     return {FAMILIES[i]: (ms[i], n[i]) for i in range(SF_K_COUNT) if n[i] > 0}
 
 
-def sfk_gemm_bf16(stream, X, rows_cap, W, M, K, count, dense_count, Y, ldy, splits, ws=None, tile_ctr=None,
-                  err=None) -> None:
+def sfk_gemm_bf16(stream, X, rows_cap, W, M, K, count, dense_count, Y, ldy, splits, err=None) -> None:
     _check(lib.sfk_gemm_bf16(stream, X, int(rows_cap), W, int(M), int(K), count, int(dense_count), Y, int(ldy),
-                             int(splits), ws, tile_ctr, err), None, "sfk_gemm_bf16")
+                             int(splits), err), None, "sfk_gemm_bf16")
 
 
 # ---------------------------------------------------------------- torch convenience

@@ -57,8 +57,7 @@ void free_ctx(sf_ctx* c) {
   for (auto& L : c->layers) {
     cudaFree(L.wqkv); cudaFree(L.wo); cudaFree(L.wgu); cudaFree(L.wd); cudaFree(L.g1); cudaFree(L.g2);
   }
-  void* bufs[] = {c->H, c->h, c->fphys, c->xn, c->qkv, c->attn, c->u, c->y32, c->gemm_ws, c->tile_ctr,
-                  c->part_o, c->part_ml,
+  void* bufs[] = {c->H, c->h, c->fphys, c->xn, c->qkv, c->attn, c->u, c->y32, c->part_o, c->part_ml,
                   c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->err_dev, c->rope};
   for (void* b : bufs) cudaFree(b);
   if (c->err_host) cudaFreeHost(c->err_host);
@@ -131,9 +130,7 @@ cudaError_t run_gemm(sf_ctx* c, Launch& lc, int fam, const GemmArgs& g, const CU
   t.dense_count = g.dense_count;
   t.max_rows = g.max_rows;
   const int n_tiles = g.count ? 1 : (g.dense_count + 255) / 256;
-  t.splits = gemm_tc_splits(g.M, g.K, n_tiles, c->gemm_ws_floats, g.max_rows);
-  t.ws = c->gemm_ws;
-  t.tile_ctr = c->tile_ctr;
+  t.splits = gemm_tc_splits(g.M, g.K, n_tiles);
   t.err = c->err_dev;
   return launch_gemm_tc(lc, fam, t, kind, e);
 }
@@ -304,9 +301,6 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
   SF_TRY(dalloc(&c->attn, (size_t)RC * c->q_dim * ab));
   SF_TRY(dalloc(&c->u, (size_t)RC * c->Fp * ab));
   if (bf16) {
-    c->gemm_ws_floats = (size_t)8 * T * std::max(c->Mqkv_pad, d);
-    SF_TRY(dalloc(&c->gemm_ws, c->gemm_ws_floats * 4));
-    SF_TRY(dalloc(&c->tile_ctr, (size_t)(maxM / 128) * (RC / 256) * sizeof(unsigned)));
     if (!make_tmap_bf16(&c->tm_xn, c->xn, d, RC, 64) || !make_tmap_bf16(&c->tm_attn, c->attn, c->q_dim, RC, 64) ||
         !make_tmap_bf16(&c->tm_u, c->u, c->Fp, RC, 64)) {
       free_ctx(c);

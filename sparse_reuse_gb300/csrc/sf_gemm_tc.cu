@@ -4,14 +4,18 @@
 // The weight is the M operand: each CTA owns 128 output features (TMEM lanes)
 // and up to 256 rows (TMEM columns), so a weight tile is streamed once for all
 // rows of a layer; the rows are the N operand, loaded in 64-row TMA boxes only
-// up to the live row count.  Narrow GEMMs split K over CTAs; the partial sums
-// go to a workspace and the last CTA of a tile (atomic ticket, no waiting)
-// adds them in split order, so results do not depend on scheduling.
+// up to the live row count.  Narrow GEMMs split K over the CTAs of a thread
+// block cluster (along grid z); after the main loops every CTA pushes its
+// partial accumulators, 32 rows at a time, into the shared memory of the CTA
+// that owns those rows (distributed shared memory), and each owner adds the
+// partials in cluster-rank order before the epilogue, so the result does not
+// depend on scheduling and no global workspace is used.
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the
-// MMAs, warps 2-5 drain TMEM through shared memory into the layer epilogue.
+// MMAs, warps 2-5 drain TMEM into the layer epilogue.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "sf_epilogue.cuh"
@@ -31,17 +35,22 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_CHUNK = RC * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
-constexpr int STAGE_LD = 129;  // epilogue staging row stride (floats)
+constexpr int PIPE_BYTES = STAGES * (A_BYTES + B_BYTES);
+constexpr int SMEM_BYTES = PIPE_BYTES + 1024 + 256;
+constexpr int STAGE_LD = 129;            // epilogue staging row stride (floats)
+constexpr int CHUNK_BYTES = 32 * BM * 4;  // 32 rows x 128 features of fp32 partials
+
+// Split counts whose exchange buffers fit the pipeline's shared memory for a
+// full 256-row tile: S * ceil(8 / S) chunks of 32 rows.
+__host__ __device__ constexpr bool split_fits(int S) {
+  return S >= 1 && S <= 8 && S * ((8 + S - 1) / S) * CHUNK_BYTES <= PIPE_BYTES;
+}
 
 struct Params {
   int M, K;
   const int32_t* count;
   int dense_count;
-  int max_rows;
-  int splits;
-  float* ws;           // [splits][max_rows][M] partial sums (splits > 1)
-  unsigned* tile_ctr;  // [n_tiles][m_tiles] arrival tickets, zero between launches
+  int splits;  // cluster size along z (1 = no split)
   unsigned* err;
 };
 
@@ -54,23 +63,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PIPE_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
-  int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int count = p.count ? *p.count : p.dense_count;
-  const int m_tile = blockIdx.x, n_tile = blockIdx.y, z = blockIdx.z;
+  const int m_tile = blockIdx.x, n_tile = blockIdx.y;
+  const int S = p.splits;
+  const int z = S > 1 ? (int)cluster_ctarank() : 0;
   const int row0 = n_tile * BN;
-  if (row0 >= count) return;
+  if (row0 >= count) return;  // uniform over the cluster (same n_tile)
   const int n_rows = min(BN, count - row0);
   const int n_mma = (n_rows + 15) & ~15;
   const int n_chunks = (n_rows + RC - 1) / RC;
   const int nk = p.K / BK;
-  const int kb0 = (int)((long long)z * nk / p.splits);
-  const int kb1 = (int)((long long)(z + 1) * nk / p.splits);
+  const int kb0 = (int)((long long)z * nk / S);
+  const int kb1 = (int)((long long)(z + 1) * nk / S);
   const int m0 = m_tile * BM;
 
   if (threadIdx.x == 0) {
@@ -86,6 +96,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  const int q = warp & 3;
+  const int f = q * 32 + lane;
+  const int ew = warp - 2;
+  const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+  bool go = true;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -99,9 +114,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < n_chunks; ++c)
           tma_load_2d(sB + s * B_BYTES + c * B_CHUNK, &tmB, kb * BK, row0 + c * RC, &full[s]);
       }
-      // every copy this CTA issued lands before it can exit
+      // every copy this CTA issued lands before its shared memory is reused
       for (int j = max(0, it - STAGES); j < it; ++j) mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.err);
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
@@ -119,52 +135,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_commit(&empty[s]);
       }
       mma_commit(tfull);
-      // TMEM is released only after every MMA of this CTA has completed
+      // TMEM and shared memory are reused only after every MMA has completed
       mbar_wait(tfull, 0, p.err);
     }
     __syncwarp();
   } else {
-    const int q = warp & 3;
-    const int f = q * 32 + lane;
-    const int ew = warp - 2;
-    float* stage = reinterpret_cast<float*>(smem);
-    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-    bool go = mbar_wait(tfull, 0, p.err);
+    go = mbar_wait(tfull, 0, p.err);
     fence_after_sync();
-    if (go && p.splits > 1) {
+    if (S == 1 && go) {
+      float* stage = reinterpret_cast<float*>(smem);
       for (int j0 = 0; j0 < n_rows; j0 += 32) {
         float v[32];
         tmem_ld32(tbase + j0, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j0 + j < n_rows) p.ws[((size_t)z * p.max_rows + row0 + j0 + j) * p.M + m0 + f] = v[j];
-      }
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 64) {
-        unsigned* ctr = p.tile_ctr + (size_t)n_tile * gridDim.x + m_tile;
-        const unsigned t = atomicAdd(ctr, 1u);
-        *last_flag = (t == (unsigned)p.splits - 1) ? 1 : 0;
-        if (*last_flag) *ctr = 0u;
-      }
-      named_bar_sync(1, 128);
-      go = *last_flag != 0;
-      if (go) __threadfence();
-    }
-    if (go) {
-      for (int j0 = 0; j0 < n_rows; j0 += 32) {
-        float v[32];
-        if (p.splits == 1) {
-          tmem_ld32(tbase + j0, v);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
-          for (int s = 0; s < p.splits; ++s) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j0 + j < n_rows) v[j] += __ldcg(p.ws + ((size_t)s * p.max_rows + row0 + j0 + j) * p.M + m0 + f);
-          }
-        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) stage[j * STAGE_LD + f] = v[j];
         named_bar_sync(1, 128);
@@ -175,6 +157,43 @@ __global__ void __launch_bounds__(THREADS, 1)
           Epi::apply(ep, row0 + j0 + jj, m0, lane, vv);
         }
         named_bar_sync(1, 128);
+      }
+    }
+  }
+
+  if (S > 1) {
+    // chunk c (32 rows) belongs to cluster rank c % S, which keeps the
+    // partials of every rank for it at buf[rank][c / S][row][feature]
+    const int nc = (n_rows + 31) / 32;
+    const int n_own = (nc + S - 1) / S;
+    float* buf = reinterpret_cast<float*>(smem);
+    if (threadIdx.x == 0 && (size_t)S * n_own * CHUNK_BYTES > (size_t)PIPE_BYTES) raise_error(p.err, kErrGemm);
+    fence_before_sync();
+    cluster_sync_all();  // every CTA of the tile is past its main loop
+    if (warp >= 2 && go && (size_t)S * n_own * CHUNK_BYTES <= (size_t)PIPE_BYTES) {
+      for (int c = 0; c < nc; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        const uint32_t local = smem_u32(buf + ((size_t)(z * n_own + c / S) * 32) * BM + f);
+        const uint32_t remote = map_to_rank(local, (uint32_t)(c % S));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_cluster_f32(remote + j * BM * 4, v[j]);
+      }
+    }
+    cluster_sync_all();  // every partial has been delivered
+    if (warp >= 2 && (size_t)S * n_own * CHUNK_BYTES <= (size_t)PIPE_BYTES) {
+      for (int lc = 0; lc < n_own; ++lc) {
+        const int c = z + lc * S;
+        if (c >= nc) break;
+        for (int jj = ew; jj < 32 && c * 32 + jj < n_rows; jj += 4) {
+          float vv[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int s = 0; s < S; ++s) {
+            const float* src = buf + ((size_t)(s * n_own + lc) * 32 + jj) * BM + lane;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) vv[cc] += src[32 * cc];
+          }
+          Epi::apply(ep, row0 + c * 32 + jj, m0, lane, vv);
+        }
       }
     }
   }
@@ -240,51 +259,61 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int gemm_tc_splits(int M, int K, int n_tiles, size_t ws_floats, int max_rows) {
+int gemm_tc_splits(int M, int K, int n_tiles) {
   const int m_tiles = M / tc::BM, nk = K / tc::BK;
-  int s = sm_count() / std::max(1, m_tiles * n_tiles);
-  s = std::min(s, std::max(1, nk / 2));
-  s = std::min(s, 16);
-  const size_t per = (size_t)max_rows * M;
-  if (per > 0) s = (int)std::min<size_t>((size_t)s, ws_floats / per);
-  return std::max(1, s);
+  const int want = std::min(sm_count() / std::max(1, m_tiles * n_tiles), nk);
+  for (int s = 8; s > 1; --s)
+    if (s <= want && tc::split_fits(s)) return s;
+  return 1;
 }
 
+namespace {
+
+template <class Epi>
+cudaError_t launch_tc(const TcGemm& g, const typename Epi::Params& ep, cudaStream_t st) {
+  cudaError_t e = set_smem_attr<Epi>();
+  if (e != cudaSuccess) return e;
+  tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g.M / tc::BM, (g.max_rows + tc::BN - 1) / tc::BN, g.splits);
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)g.splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p, ep);
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_tc(Launch& lc, int fam, const TcGemm& g, EpiKind kind, const EpiArgs& e) {
-  if (g.M % tc::BM != 0 || g.K % tc::BK != 0 || g.splits < 1 || g.splits > g.K / tc::BK) return cudaErrorInvalidValue;
-  tc::Params p{g.M, g.K, g.count, g.dense_count, g.max_rows, g.splits, g.ws, g.tile_ctr, g.err};
-  dim3 grid(g.M / tc::BM, (g.max_rows + tc::BN - 1) / tc::BN, g.splits);
+  if (g.M % tc::BM != 0 || g.K % tc::BK != 0 || !tc::split_fits(g.splits) || g.splits > g.K / tc::BK)
+    return lc.err = cudaErrorInvalidValue;
   cudaError_t err = cudaSuccess;
   lc.before(fam);
   switch (kind) {
     case kEpiQKV: {
       using E = EpiQKV<__nv_bfloat16>;
-      E::Params ep{(__nv_bfloat16*)e.qkv, e.qkv_ld, e.qk_dim, e.qkv_M, e.hd, e.rc, e.L, e.P, e.rope};
-      err = set_smem_attr<E>();
-      if (err == cudaSuccess) tc::gemm_tc_kernel<E><<<grid, tc::THREADS, tc::SMEM_BYTES, lc.st>>>(*g.tmA, *g.tmB, p, ep);
+      err = launch_tc<E>(g, E::Params{(__nv_bfloat16*)e.qkv, e.qkv_ld, e.qk_dim, e.qkv_M, e.hd, e.rc, e.L, e.P, e.rope},
+                         lc.st);
       break;
     }
-    case kEpiResidual: {
-      using E = EpiResidual;
-      E::Params ep{e.h, e.H, e.h_ld};
-      err = set_smem_attr<E>();
-      if (err == cudaSuccess) tc::gemm_tc_kernel<E><<<grid, tc::THREADS, tc::SMEM_BYTES, lc.st>>>(*g.tmA, *g.tmB, p, ep);
+    case kEpiResidual:
+      err = launch_tc<EpiResidual>(g, EpiResidual::Params{e.h, e.H, e.h_ld}, lc.st);
       break;
-    }
     case kEpiSwiGLU: {
       using E = EpiSwiGLU<__nv_bfloat16>;
-      E::Params ep{(__nv_bfloat16*)e.u, e.u_ld};
-      err = set_smem_attr<E>();
-      if (err == cudaSuccess) tc::gemm_tc_kernel<E><<<grid, tc::THREADS, tc::SMEM_BYTES, lc.st>>>(*g.tmA, *g.tmB, p, ep);
+      err = launch_tc<E>(g, E::Params{(__nv_bfloat16*)e.u, e.u_ld}, lc.st);
       break;
     }
-    case kEpiStore: {
-      using E = EpiStore;
-      E::Params ep{e.y, e.y_ld};
-      err = set_smem_attr<E>();
-      if (err == cudaSuccess) tc::gemm_tc_kernel<E><<<grid, tc::THREADS, tc::SMEM_BYTES, lc.st>>>(*g.tmA, *g.tmB, p, ep);
+    case kEpiStore:
+      err = launch_tc<EpiStore>(g, EpiStore::Params{e.y, e.y_ld}, lc.st);
       break;
-    }
   }
   if (err != cudaSuccess && lc.err == cudaSuccess) lc.err = err;
   lc.after(fam);
@@ -294,17 +323,16 @@ cudaError_t launch_gemm_tc(Launch& lc, int fam, const TcGemm& g, EpiKind kind, c
 }  // namespace sf
 
 extern "C" sf_status sfk_gemm_bf16(void* stream, const void* X, int rows_cap, const void* W, int M, int K,
-                                   const int32_t* count, int dense_count, float* Y, int ldy, int splits, float* ws,
-                                   uint32_t* tile_ctr, uint32_t* err) {
+                                   const int32_t* count, int dense_count, float* Y, int ldy, int splits,
+                                   uint32_t* err) {
   using namespace sf;
   if (!X || !W || !Y || rows_cap <= 0 || M <= 0 || K <= 0 || M % tc::BM != 0 || K % tc::BK != 0 || ldy < M ||
-      splits < 1 || splits > K / tc::BK || (splits > 1 && (!ws || !tile_ctr)) || (!count && dense_count > rows_cap) ||
-      dense_count < 0)
+      !tc::split_fits(splits) || splits > K / tc::BK || (!count && dense_count > rows_cap) || dense_count < 0)
     return SF_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(X) & 15u) || (reinterpret_cast<uintptr_t>(W) & 15u)) return SF_ERR_INVALID_ARG;
   alignas(64) CUtensorMap tmA, tmB;
   if (!make_tmap_bf16(&tmA, W, K, M, tc::BM) || !make_tmap_bf16(&tmB, X, K, rows_cap, tc::RC)) return SF_ERR_CUDA;
-  TcGemm g{&tmA, &tmB, M, K, count, dense_count, rows_cap, splits, ws, tile_ctr, err};
+  TcGemm g{&tmA, &tmB, M, K, count, dense_count, rows_cap, splits, err};
   EpiArgs e{};
   e.y = Y;
   e.y_ld = ldy;

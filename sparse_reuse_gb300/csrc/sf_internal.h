@@ -62,9 +62,6 @@ struct sf_ctx {
   void* u = nullptr;        // [T_max][Fp] SwiGLU activations of the recompute rows
   float* y32 = nullptr;     // [T_max][max M] fp32 GEMM accumulators (FP32 contexts)
   int rows_cap = 0;         // activation buffers' row capacity (T_max rounded to 256)
-  float* gemm_ws = nullptr; // split-K partial sums of the tcgen05 GEMM
-  size_t gemm_ws_floats = 0;
-  unsigned* tile_ctr = nullptr;  // split-K arrival tickets
   alignas(64) CUtensorMap tm_xn, tm_attn, tm_u;  // activation operands (BF16 contexts)
   float* part_o = nullptr;  // [max_splits][T_max][nq][hd] prefix-attention partials
   float* part_ml = nullptr; // [max_splits][T_max][nq][2]  (running max, denominator)
@@ -176,13 +173,11 @@ struct TcGemm {
   const int32_t* count;
   int dense_count;
   int max_rows;
-  int splits;
-  float* ws;
-  unsigned* tile_ctr;
+  int splits;  // K split over a cluster of this many CTAs (1..6 or 8)
   unsigned* err;
 };
 bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
-int gemm_tc_splits(int M, int K, int n_tiles, size_t ws_floats, int max_rows);
+int gemm_tc_splits(int M, int K, int n_tiles);
 cudaError_t launch_gemm_tc(Launch& lc, int fam, const TcGemm& g, EpiKind kind, const EpiArgs& e);
 
 // sf_gemm.cu (FP32 contexts)

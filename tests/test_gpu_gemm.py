@@ -23,17 +23,11 @@ def _run(sf, M, K, rows_cap, count, splits, on_device=True, seed=0):
     W = (torch.randn((M, K), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
     Y = torch.full((rows_cap, M), float("nan"), device="cuda")
     cnt = torch.tensor([count], dtype=torch.int32, device="cuda")
-    n_tiles = (rows_cap + 255) // 256
-    ws = torch.zeros((splits, rows_cap, M), device="cuda") if splits > 1 else None
-    ctr = torch.zeros((n_tiles * (M // 128),), dtype=torch.int32, device="cuda") if splits > 1 else None
     err = torch.zeros((1,), dtype=torch.int32, device="cuda")
-    p = lambda t: None if t is None else t.data_ptr()
     sf.sfk_gemm_bf16(None, X.data_ptr(), rows_cap, W.data_ptr(), M, K, cnt.data_ptr() if on_device else None,
-                     count, Y.data_ptr(), M, splits, p(ws), p(ctr), err.data_ptr())
+                     count, Y.data_ptr(), M, splits, err.data_ptr())
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    if ctr is not None:
-        assert int(ctr.abs().sum().item()) == 0     # tickets are left at zero
     ref = X[:count].double().cpu().numpy() @ W.double().cpu().numpy().T
     got = Y[:count].double().cpu().numpy()
     scale = np.abs(X[:count].double().cpu().numpy()) @ np.abs(W.double().cpu().numpy().T) + 1e-30
@@ -47,10 +41,11 @@ def test_counts_single_split(sf, count):
     _run(sf, 256, 512, 512, count, 1)
 
 
-@pytest.mark.parametrize("splits", [2, 3, 7, 8])
+@pytest.mark.parametrize("splits", [2, 3, 4, 5, 6, 8])
 def test_split_k(sf, splits):
     _run(sf, 384, 1536, 300, 288, splits)
     _run(sf, 384, 1536, 300, 50, splits, seed=1)
+    _run(sf, 128, 1024, 256, 256, splits, seed=2)
 
 
 def test_zero_rows_writes_nothing(sf):
@@ -59,7 +54,7 @@ def test_zero_rows_writes_nothing(sf):
 
 
 def test_dense_count_and_long_k(sf):
-    _run(sf, 128, 8960, 64, 50, 12, on_device=False)
+    _run(sf, 128, 8960, 64, 50, 8, on_device=False)
     _run(sf, 1536, 1536, 288, 288, 4, on_device=False)
 
 
@@ -73,4 +68,6 @@ def test_bad_arguments_rejected(sf):
     with pytest.raises(sf.SpecFoldError):
         sf.sfk_gemm_bf16(None, 16, 64, 16, 100, 64, None, 1, 16, 100, 1)      # M not a multiple of 128
     with pytest.raises(sf.SpecFoldError):
-        sf.sfk_gemm_bf16(None, 16, 64, 16, 128, 64, None, 1, 16, 128, 2)      # split without workspace
+        sf.sfk_gemm_bf16(None, 16, 64, 16, 128, 64, None, 1, 16, 128, 2)      # more splits than K blocks
+    with pytest.raises(sf.SpecFoldError):
+        sf.sfk_gemm_bf16(None, 16, 64, 16, 128, 1024, None, 1, 16, 128, 7)    # cluster size without room
