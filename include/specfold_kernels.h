@@ -38,6 +38,44 @@ sf_status sfk_gemm_bf16(void* stream, const void* X, int rows_cap, const void* W
                         const int32_t* count, int dense_count, float* Y, int ldy, int splits,
                         uint32_t* err);
 
+/* Allocation-free form of the first layer's gate, compaction and source
+ * resolution (the step sf_verify runs at layer 0).  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc or any allocating library routine: for example a plugin inside
+ * an inference engine that owns all device memory through a fixed arena, a
+ * latency-critical serving loop that bans allocator calls (they can block on
+ * the device), or code that must run while a CUDA stream is being captured
+ * into a graph.  It allocates nothing: the kernel's scratch (arrival ticket,
+ * fold-flag staging, per-request offset table, error word; 12,800 bytes) is a
+ * file-scope __device__ array that every GPU which loads the library holds
+ * until the process exits.
+ *
+ *   hidden    device [R, B+1, L, d] in dtype (SF_F32 or SF_BF16): the block's
+ *             layer-0 input; d a multiple of 4, rows 16-byte aligned.
+ *   parent    HOST int32 [R, B+1], same rules as sf_verify.
+ *   delta     >= 0 and finite; 0 means nothing folds.
+ * Outputs (device, caller-owned, all required), T = R * (B+1) * L:
+ *   H_out     fp32 [T, d]: the input converted to fp32.
+ *   fold      uint8 [T]: 1 = folded.
+ *   rc        int32 [T]: ascending recompute row ids (r*(B+1)+i)*L+n; the
+ *             first *rc_count entries are written.
+ *   rcslot    int32 [T]: index in rc of each row's resolved source.
+ *   src       int32 [T]: resolved source branch of each row.
+ *   rc_count  int32 [1]: size of the recompute set.
+ * Limits (SF_ERR_SHAPE beyond them): T <= 8192, R * (B+1) <= 1024, B+1 <= 127.
+ * Errors returned before anything is enqueued: SF_ERR_INVALID_ARG,
+ * SF_ERR_SHAPE, SF_ERR_TREE; SF_ERR_CUDA if the set-up or launch fails.
+ *
+ * The first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Every call on a device shares the one array, and the call clears the parts
+ * that must start at zero: calls that overlap on the GPU (different streams,
+ * or host threads without ordering) race on it and must be serialised by the
+ * caller. */
+sf_status sfk_gate_noalloc(void* stream, const void* hidden, int dtype, const int32_t* parent, int R, int B,
+                           int L, int d, float delta, float* H_out, uint8_t* fold, int32_t* rc, int32_t* rcslot,
+                           int32_t* src, int32_t* rc_count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ SF_K_COUNT = len(FAMILIES)
 # every symbol include/specfold.h declares
 EXPORTS = ["sf_create", "sf_verify", "sf_set_debug", "sf_sync_status", "sf_destroy", "sf_status_str",
            "sf_last_error", "sf_get_stats", "sf_set_graphs", "sf_timing_begin", "sf_timing_read",
-           "sfk_gemm_bf16"]
+           "sfk_gemm_bf16", "sfk_gate_noalloc"]
 
 
 class SfShapes(ctypes.Structure):
@@ -74,6 +74,8 @@ def _load() -> ctypes.CDLL:
     lib.sf_timing_begin.argtypes = [vp, ctypes.c_uint]
     lib.sf_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
     lib.sfk_gemm_bf16.argtypes = [vp, vp, c_int, vp, c_int, c_int, vp, c_int, vp, c_int, c_int, vp]
+    lib.sfk_gate_noalloc.argtypes = [vp, vp, c_int, i32p, c_int, c_int, c_int, c_int, c_float, vp, vp, vp, vp, vp,
+                                     vp]
     for name in EXPORTS:
         fn = getattr(lib, name)
         if name not in ("sf_status_str", "sf_last_error"):
@@ -176,6 +178,14 @@ def sf_timing_read(ctx) -> dict:
 def sfk_gemm_bf16(stream, X, rows_cap, W, M, K, count, dense_count, Y, ldy, splits, err=None) -> None:
     _check(lib.sfk_gemm_bf16(stream, X, int(rows_cap), W, int(M), int(K), count, int(dense_count), Y, int(ldy),
                              int(splits), err), None, "sfk_gemm_bf16")
+
+
+def sfk_gate_noalloc(stream, hidden, dtype, parent, R, B, L, d, delta, H_out, fold, rc, rcslot, src,
+                     rc_count) -> None:
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    _check(lib.sfk_gate_noalloc(stream, hidden, int(dtype), par.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                int(R), int(B), int(L), int(d), float(delta), H_out, fold, rc, rcslot, src,
+                                rc_count), None, "sfk_gate_noalloc")
 
 
 # ---------------------------------------------------------------- torch convenience

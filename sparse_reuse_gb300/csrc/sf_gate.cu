@@ -9,7 +9,11 @@
 // bypasses the gate.  Compaction: App. B, recomputed indices go to a global
 // and per-branch list.  Resolution: §A.3 / App. B, a folded position follows
 // its chain to the nearest ancestor that recomputed it.
+#include <cmath>
+#include <mutex>
+
 #include "sf_internal.h"
+#include "specfold_kernels.h"
 
 namespace sf {
 namespace {
@@ -287,4 +291,90 @@ cudaError_t launch_pack_transpose(cudaStream_t st, const void* src, int K, int N
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free entry point of the gate / compaction / resolution step.
+//
+// The kernel above needs a little scratch besides its inputs and outputs: the
+// arrival ticket that elects the last block, the fold flags the last block
+// re-reads, the per-request offset table and a device error word.  Here that
+// scratch is one file-scope device array, so the call allocates nothing.
+
+namespace {
+
+constexpr size_t kScratchTicket = 0;                        // unsigned
+constexpr size_t kScratchErr = 4;                           // unsigned
+constexpr size_t kScratchMeta = 256;                        // int32 [2 + kMaxTreeSlots]
+constexpr size_t kScratchFlags = kScratchMeta + 4352;       // uint8 [kMaxRows]
+constexpr size_t kScratchBytes = kScratchFlags + sf::kMaxRows;  // 12800 bytes
+
+// Shared by every call on a device and kept until the process exits.
+static __device__ __align__(256) unsigned char g_gate_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+unsigned char* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_gate_scratch on the current device (looked up once per
+// device; the host-side symbol itself is not a device address).
+cudaError_t gate_scratch(unsigned char** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gate_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
 }  // namespace sf
+
+extern "C" sf_status sfk_gate_noalloc(void* stream, const void* hidden, int dtype, const int32_t* parent, int R,
+                                      int B, int L, int d, float delta, float* H_out, uint8_t* fold, int32_t* rc,
+                                      int32_t* rcslot, int32_t* src, int32_t* rc_count) {
+  using namespace sf;
+  if (!hidden || !parent || !H_out || !fold || !rc || !rcslot || !src || !rc_count) return SF_ERR_INVALID_ARG;
+  if ((dtype != SF_F32 && dtype != SF_BF16) || R < 1 || B < 0 || L < 1 || d <= 0 || d % 4 != 0 ||
+      !std::isfinite(delta) || delta < 0.f)
+    return SF_ERR_INVALID_ARG;
+  const int Bp = B + 1;
+  if (Bp > 127 || (long)R * Bp > kMaxTreeSlots || (long)R * Bp * L > kMaxRows) return SF_ERR_SHAPE;
+  for (int r = 0; r < R; ++r) {
+    if (parent[r * Bp] != -1) return SF_ERR_TREE;
+    for (int i = 1; i < Bp; ++i)
+      if (parent[r * Bp + i] < 0 || parent[r * Bp + i] >= i) return SF_ERR_TREE;
+  }
+  unsigned char* scratch = nullptr;
+  if (gate_scratch(&scratch) != cudaSuccess) return SF_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the ticket and the error word must start at zero; the rest is overwritten
+  if (cudaMemsetAsync(scratch, 0, 8, st) != cudaSuccess) return SF_ERR_CUDA;
+  GateArgs a{};
+  a.tree.R = R;
+  a.tree.Bp = Bp;
+  for (int k = 0; k < R * Bp; ++k) a.tree.parent[k] = (int8_t)parent[k];
+  a.x_in = hidden;
+  a.H_out = H_out;
+  a.fold = scratch + kScratchFlags;
+  a.fold_user = fold;
+  a.rc = rc;
+  a.rcslot = rcslot;
+  a.src_user = src;
+  a.meta = reinterpret_cast<int32_t*>(scratch + kScratchMeta);
+  a.rc_count_user = rc_count;
+  a.ticket = reinterpret_cast<unsigned*>(scratch + kScratchTicket);
+  a.err = reinterpret_cast<unsigned*>(scratch + kScratchErr);
+  a.delta = delta;
+  a.T = R * Bp * L;
+  a.d = d;
+  a.L = L;
+  Launch lc{nullptr, st};
+  launch_gate(lc, a, dtype == SF_BF16);
+  return lc.err == cudaSuccess ? SF_OK : SF_ERR_CUDA;
+}
