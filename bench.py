@@ -175,6 +175,10 @@ def main():
     ap.add_argument("--drafts", type=int, default=None)
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling only: run the first N layers of the config")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="profiling only: warm-up and timed passes, nothing else, no JSON line")
     args = ap.parse_args()
 
     import torch
@@ -191,6 +195,8 @@ def main():
     cfg = synth.CONFIGS[args.config]
     if args.drafts is not None:
         cfg = cfg.with_(n_drafts=args.drafts)
+    if args.layers is not None:
+        cfg = cfg.with_(n_layers=args.layers)
     delta = cfg.delta if args.delta is None else args.delta
     config = {"workload": workload_desc(cfg), "R": cfg.n_requests, "B": cfg.n_drafts, "L": cfg.block_len,
               "P": cfg.prefix_len, "layers": cfg.n_layers, "d_model": cfg.d_model, "delta": delta,
@@ -260,6 +266,10 @@ def main():
             ms = float(t.item())
         return ms, ctx.stats()["kernel_launches"] - s0
 
+    if args.profile_only:
+        timed(delta, args.steps, args.warmup)
+        ctx.close()
+        return
     with ClockSampler(local) as clk:
         ms, launches = timed(delta, args.steps, args.warmup)
     rc_fold = rcc.cpu().numpy().tolist()

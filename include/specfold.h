@@ -170,9 +170,11 @@ sf_status sf_get_stats(const sf_ctx* ctx, sf_stats* out);
  * Never used while the caller's stream is itself being captured. */
 sf_status sf_set_graphs(sf_ctx* ctx, int use_graphs);
 
-/* Per-family timing: while family_mask != 0, sf_verify launches directly (no
- * graph) and brackets every launch of the selected families with CUDA events
- * on the call's stream.  sf_timing_read synchronises those events and returns
+/* Per-family timing: while family_mask != 0, every sf_verify call records the
+ * pass into a fresh CUDA graph with an event-record node before and after
+ * every launch of the selected families, and replays it on the call's stream
+ * (on the legacy default stream the kernels are launched directly between
+ * event records instead).  sf_timing_read synchronises those events and returns
  * per family the summed milliseconds and the number of launches since the
  * last sf_timing_begin.  total_ms and launches have SF_K_COUNT entries. */
 sf_status sf_timing_begin(sf_ctx* ctx, unsigned family_mask);

@@ -64,6 +64,7 @@ void free_ctx(sf_ctx* c) {
   for (auto e : c->ev_start) cudaEventDestroy(e);
   for (auto e : c->ev_stop) cudaEventDestroy(e);
   if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+  if (c->timing_exec) cudaGraphExecDestroy(c->timing_exec);
   delete c;
 }
 
@@ -84,7 +85,10 @@ void Launch::before(int fam) {
       ctx->ev_family.push_back(fam);
     }
     ctx->ev_family[ctx->ev_used] = fam;
-    cudaEventRecord(ctx->ev_start[ctx->ev_used], st);
+    if (external_events)
+      cudaEventRecordWithFlags(ctx->ev_start[ctx->ev_used], st, cudaEventRecordExternal);
+    else
+      cudaEventRecord(ctx->ev_start[ctx->ev_used], st);
   }
 }
 
@@ -94,7 +98,10 @@ void Launch::after(int fam) {
   ++launches;
   ++family[fam];
   if (ctx && ctx->timing_mask & (1u << fam)) {
-    cudaEventRecord(ctx->ev_stop[ctx->ev_used], st);
+    if (external_events)
+      cudaEventRecordWithFlags(ctx->ev_stop[ctx->ev_used], st, cudaEventRecordExternal);
+    else
+      cudaEventRecord(ctx->ev_stop[ctx->ev_used], st);
     ++ctx->ev_used;
   }
 }
@@ -140,12 +147,6 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
   const int Bp = p.B + 1, L = s.block_len, T = p.R * Bp * L, d = s.d_model;
   const int nl = s.n_layers, bf16 = s.dtype == SF_BF16;
   const size_t kv_layer = (size_t)p.R * p.P * s.n_kv_heads * s.head_dim * c->act_bytes;
-  int n_splits = 0, split_len = 0;
-  if (p.P > 0) {
-    n_splits = std::min(c->max_splits, (p.P + 63) / 64);
-    split_len = round_up((p.P + n_splits - 1) / n_splits, 32);
-    n_splits = (p.P + split_len - 1) / split_len;
-  }
   GateArgs ga{};
   ga.tree.R = p.R;
   ga.tree.Bp = Bp;
@@ -194,7 +195,7 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     a.attn = c->attn; a.ld_attn = c->q_dim;
     a.R = p.R; a.Bp = Bp; a.L = L; a.P = p.P; a.T = T;
     a.nq = s.n_q_heads; a.nkv = s.n_kv_heads; a.hd = s.head_dim;
-    a.n_splits = n_splits; a.split_len = split_len;
+    a.target_ctas = c->sm_count;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
     a.err = c->err_dev;
     if (launch_attention(lc, bf16, a) != cudaSuccess) return lc.err;
@@ -278,6 +279,8 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
   c->T_max = s.max_requests * s.max_branches * s.block_len;
   c->max_pos = s.max_prefix + s.block_len;
   c->max_splits = 8;
+  cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+  if (c->sm_count <= 0) c->sm_count = 148;
   const int d = s.d_model, T = c->T_max, ab = c->act_bytes;
   const size_t maxM = (size_t)std::max(std::max(c->Mqkv_pad, c->Mgu), d);
   cudaError_t e = cudaSuccess;
@@ -427,6 +430,35 @@ sf_status sf_verify(sf_ctx* c, void* stream, const void* hidden_in, const int32_
     c->stats.graph_replays++;
     c->stats.kernel_launches += c->graph_nodes;
     for (int f = 0; f < SF_K_COUNT; ++f) c->stats.family_launches[f] += c->graph_family[f];
+    return SF_OK;
+  }
+  if (c->timing_mask != 0 && st != nullptr && cap == cudaStreamCaptureStatusNone) {
+    // timed pass: the same kernels as a graph replay, with an event-record
+    // node around every launch of the selected families, so the events see
+    // back-to-back device execution rather than host launch gaps
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    Launch lc{c, st};
+    lc.external_events = true;
+    cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) enqueue_pass(c, lc, pa);
+    cudaError_t e2 = e == cudaSuccess ? cudaStreamEndCapture(st, &graph) : e;
+    if (e == cudaSuccess && lc.err == cudaSuccess && e2 == cudaSuccess) e2 = cudaGraphInstantiate(&exec, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess || lc.err != cudaSuccess || e2 != cudaSuccess) {
+      cudaGetLastError();
+      return fail(c, SF_ERR_CUDA, "timing capture failed: %s",
+                  cudaGetErrorString(e != cudaSuccess ? e : (lc.err != cudaSuccess ? lc.err : e2)));
+    }
+    e = cudaGraphLaunch(exec, st);
+    if (c->timing_exec) {
+      cudaStreamSynchronize(st);
+      cudaGraphExecDestroy(c->timing_exec);
+    }
+    c->timing_exec = exec;
+    if (e != cudaSuccess) return fail(c, SF_ERR_CUDA, "timing graph launch: %s", cudaGetErrorString(e));
+    add_stats(c, lc);
+    c->stats.passes++;
     return SF_OK;
   }
   Launch lc{c, st};

@@ -9,24 +9,487 @@
 // Decomposition used here (same result, different order of work):
 //   1. prefix partial per recomputed query: streaming softmax state
 //      (max, denominator, unnormalised output) of q against the request's
-//      prefix keys, split over the prefix;
+//      prefix keys, the prefix split over S chunks;
 //   2. per (row, head): the query is the one of the row's resolved source;
 //      its block part runs over the branch's own L block keys/values, read
 //      through the source slots of the branch's positions, and is merged with
 //      the query's prefix partials by log-sum-exp.
+// The split count S is derived on the device from the live recompute count,
+// identically in both kernels, so small recompute sets still fill the GPU and
+// large ones do not pay for partials they do not need.
+//
+// BF16 contexts run both kernels on the tensor cores (mma.sync m16n8k16, bf16
+// in, fp32 accumulate); the GQA group's query heads are packed into the M
+// dimension so every key/value tile is read once per KV head.  FP32 contexts
+// use CUDA-core kernels that keep fp32 operands.
 #include "sf_internal.h"
 
 namespace sf {
 namespace {
 
 constexpr int kMaxHd = 128;
+constexpr int kMaxSplits = 8;
+constexpr int kQT = 64;  // query vectors per CTA (16 per warp)
+constexpr int kKB = 64;  // keys per block
+
+// Number of prefix splits and keys per split for this pass (device side).
+struct Splits {
+  int S, len;
+};
+
+__device__ __forceinline__ Splits prefix_splits(const AttnArgs& a) {
+  if (a.P <= 0) return {0, 0};
+  const int G = a.nq / a.nkv;
+  int tiles = 0;
+  for (int r = 0; r < a.R; ++r) tiles += (((a.meta[2 + r] - a.meta[1 + r]) * G) + kQT - 1) / kQT;
+  tiles *= a.nkv;
+  int S = tiles > 0 ? (a.target_ctas + tiles - 1) / tiles : 1;
+  S = max(1, min(S, min(kMaxSplits, (a.P + kKB - 1) / kKB)));
+  const int len = (((a.P + S - 1) / S) + kKB - 1) / kKB * kKB;
+  return {(a.P + len - 1) / len, len};
+}
+
+// ------------------------------------------------------------ tensor-core path
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float x) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(x) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Scores of this warp's 16 query rows against 64 keys in smem (rows = keys).
+template <int HD>
+__device__ __forceinline__ void qk_scores(float (&sc)[kKB / 8][4], const uint32_t (&qf)[HD / 16][4], const bf16* K,
+                                          int lane) {
+  constexpr int LD = HD + 8;
+#pragma unroll
+  for (int nt = 0; nt < kKB / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  const int j = lane >> 3;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+    for (int n2 = 0; n2 < kKB / 16; ++n2) {
+      uint32_t kf[4];
+      ldsm_x4(kf, K + (n2 * 16 + (j >> 1) * 8 + (lane & 7)) * LD + kk * 16 + (j & 1) * 8);
+      mma16816(sc[2 * n2], qf[kk], kf[0], kf[1]);
+      mma16816(sc[2 * n2 + 1], qf[kk], kf[2], kf[3]);
+    }
+  }
+}
+
+// o += P V for this warp's 16 rows; P in the score accumulators (bf16-rounded).
+template <int HD>
+__device__ __forceinline__ void pv_accum(float (&o)[HD / 8][4], const float (&p)[kKB / 8][4], const bf16* V,
+                                         int lane) {
+  constexpr int LD = HD + 8;
+  const int j = lane >> 3;
+#pragma unroll
+  for (int kt = 0; kt < kKB / 16; ++kt) {
+    uint32_t pa[4] = {pack_bf16(p[2 * kt][0], p[2 * kt][1]), pack_bf16(p[2 * kt][2], p[2 * kt][3]),
+                      pack_bf16(p[2 * kt + 1][0], p[2 * kt + 1][1]), pack_bf16(p[2 * kt + 1][2], p[2 * kt + 1][3])};
+#pragma unroll
+    for (int d2 = 0; d2 < HD / 16; ++d2) {
+      uint32_t vf[4];
+      ldsm_x4_t(vf, V + (kt * 16 + (j & 1) * 8 + (lane & 7)) * LD + d2 * 16 + (j >> 1) * 8);
+      mma16816(o[2 * d2], pa, vf[0], vf[1]);
+      mma16816(o[2 * d2 + 1], pa, vf[2], vf[3]);
+    }
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HD / 16][4], const bf16* Q, int warp, int lane) {
+  constexpr int LD = HD + 8;
+  const int j = lane >> 3;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk)
+    ldsm_x4(qf[kk], Q + (warp * 16 + (j & 1) * 8 + (lane & 7)) * LD + kk * 16 + (j >> 1) * 8);
+}
+
+// Prefix partials: CTA = (64 query vectors of one request and KV head, one
+// split of the prefix).  Query vector v of the request is recompute slot
+// off_r + v / G, query head kvh * G + v % G.  The split CTAs of a query tile
+// form one cluster (along z): after their streaming loops every CTA sends its
+// partial state (max, denominator, unnormalised output) of each query row to
+// the CTA that owns the row, and each owner merges the S states in rank order
+// and writes one merged state per query to split slot 0.
+template <int HD>
+__global__ void __launch_bounds__(128) attn_prefix_mma(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int LD = HD + 8;
+  constexpr int XLD = HD + 2;  // exchange row: o[HD], m, l
+  extern __shared__ __align__(16) unsigned char smem[];
+  bf16* sQ = reinterpret_cast<bf16*>(smem);
+  bf16* sK = sQ + kQT * LD;
+  bf16* sV = sK + 2 * kKB * LD;
+  float* xbuf = reinterpret_cast<float*>(sK);  // exchange area, reused after the loop
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
+  const Splits sp = prefix_splits(a);
+  const int G = a.nq / a.nkv;
+  const int off_r = a.meta[1 + r], nqv = (a.meta[2 + r] - off_r) * G;
+  const int q0 = blockIdx.x * kQT;
+  if (q0 >= nqv) return;  // uniform over the cluster
+  const int s = (int)cluster_rank();
+  const bool has_keys = s < sp.S;
+  const int k_lo = s * sp.len, k_hi = has_keys ? min(a.P, k_lo + sp.len) : k_lo;
+  const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
+  const bf16* pk = reinterpret_cast<const bf16*>(a.pk) + ((size_t)r * a.P * a.nkv + kvh) * HD;
+  const bf16* pv = reinterpret_cast<const bf16*>(a.pv) + ((size_t)r * a.P * a.nkv + kvh) * HD;
+  const size_t kstride = (size_t)a.nkv * HD;
+
+  float o[HD / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  if (has_keys) {
+    for (int idx = tid; idx < kQT * (HD / 8); idx += 128) {
+      const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (v < nqv) {
+        const int g = off_r + v / G, h = kvh * G + v % G;
+        val = *reinterpret_cast<const uint4*>(qkv + (size_t)g * a.ld_qkv + h * HD + c8 * 8);
+      }
+      *reinterpret_cast<uint4*>(sQ + row * LD + c8 * 8) = val;
+    }
+    auto load_kv = [&](int buf, int kb0) {
+      for (int idx = tid; idx < kKB * (HD / 8); idx += 128) {
+        const int jk = idx / (HD / 8), c8 = idx % (HD / 8), key = kb0 + jk;
+        bf16* dk = sK + (buf * kKB + jk) * LD + c8 * 8;
+        bf16* dv = sV + (buf * kKB + jk) * LD + c8 * 8;
+        if (key < k_hi) {
+          cp_async16(dk, pk + key * kstride + c8 * 8);
+          cp_async16(dv, pv + key * kstride + c8 * 8);
+        } else {
+          *reinterpret_cast<uint4*>(dk) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(dv) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      cp_async_commit();
+    };
+    const int nblk = k_hi > k_lo ? (k_hi - k_lo + kKB - 1) / kKB : 0;
+    if (nblk > 0) load_kv(0, k_lo);
+    __syncthreads();
+    uint32_t qf[HD / 16][4];
+    load_q_frags<HD>(qf, sQ, warp, lane);
+    for (int b = 0; b < nblk; ++b) {
+      if (b + 1 < nblk) {
+        load_kv((b + 1) & 1, k_lo + (b + 1) * kKB);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      float sc[kKB / 8][4];
+      qk_scores<HD>(sc, qf, sK + (b & 1) * kKB * LD, lane);
+      const int kb0 = k_lo + b * kKB;
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < kKB / 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = kb0 + nt * 8 + (lane & 3) * 2 + (e & 1);
+          sc[nt][e] = key < k_hi ? sc[nt][e] * a.scale_log2 : -INFINITY;
+        }
+        mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+      }
+      const float n0 = fmaxf(m0, quad_max(mx0)), n1 = fmaxf(m1, quad_max(mx1));
+      const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < kKB / 8; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - n0);
+        sc[nt][1] = exp2f(sc[nt][1] - n0);
+        sc[nt][2] = exp2f(sc[nt][2] - n1);
+        sc[nt][3] = exp2f(sc[nt][3] - n1);
+        s0 += sc[nt][0] + sc[nt][1];
+        s1 += sc[nt][2] + sc[nt][3];
+      }
+      l0 = l0 * c0 + s0;
+      l1 = l1 * c1 + s1;
+      m0 = n0;
+      m1 = n1;
+#pragma unroll
+      for (int nt = 0; nt < HD / 8; ++nt) {
+        o[nt][0] *= c0;
+        o[nt][1] *= c0;
+        o[nt][2] *= c1;
+        o[nt][3] *= c1;
+      }
+      pv_accum<HD>(o, sc, sV + (b & 1) * kKB * LD, lane);
+      __syncthreads();
+    }
+    l0 = quad_sum(l0);
+    l1 = quad_sum(l1);
+  }
+
+  if (sp.S == 1) {  // a single split: rank 0's partial is already the merged state
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      if (!has_keys) break;
+      const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
+      if (v >= nqv) continue;
+      const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+      float* po = a.part_o + qi * HD + (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < HD / 8; ++nt)
+        *reinterpret_cast<float2*>(po + nt * 8) = make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+      if ((lane & 3) == 0) {
+        a.part_ml[qi * 2 + 0] = half ? m1 : m0;
+        a.part_ml[qi * 2 + 1] = half ? l1 : l0;
+      }
+    }
+    return;  // uniform over the cluster: S is computed from the same counts
+  }
+  // rows [rank * per, (rank + 1) * per) of the tile are merged by `rank`
+  const int per = (kQT + sp.S - 1) / sp.S;
+  cluster_sync_all();  // every CTA is past its loop: exchange areas are free
+  if (has_keys) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int vr = warp * 16 + (lane >> 2) + half * 8;  // row within the tile
+      const int owner = vr / per;
+      const uint32_t base =
+          map_rank(smem_addr(xbuf + ((size_t)s * per + (vr - owner * per)) * XLD), (uint32_t)owner);
+#pragma unroll
+      for (int nt = 0; nt < HD / 8; ++nt)
+        st_cluster_v2(base + (nt * 8 + (lane & 3) * 2) * 4, o[nt][2 * half], o[nt][2 * half + 1]);
+      if ((lane & 3) == 0) {
+        st_cluster_f32(base + HD * 4, half ? m1 : m0);
+        st_cluster_f32(base + (HD + 1) * 4, half ? l1 : l0);
+      }
+    }
+  }
+  cluster_sync_all();  // every partial has arrived
+  if (has_keys) {
+    const int rows = min(per, kQT - s * per);
+    for (int idx = tid; idx < rows * HD; idx += 128) {
+      const int rl = idx / HD, dd = idx % HD, v = q0 + s * per + rl;
+      if (v >= nqv) continue;
+      float M = -INFINITY;
+      for (int t = 0; t < sp.S; ++t) M = fmaxf(M, xbuf[((size_t)t * per + rl) * XLD + HD]);
+      float acc = 0.f, l = 0.f;
+      for (int t = 0; t < sp.S; ++t) {
+        const float* x = xbuf + ((size_t)t * per + rl) * XLD;
+        const float w = exp2f(x[HD] - M);  // 0 for an empty split
+        acc += w * x[dd];
+        l += w * x[HD + 1];
+      }
+      const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+      a.part_o[qi * HD + dd] = acc;
+      if (dd == 0) {
+        a.part_ml[qi * 2 + 0] = M;
+        a.part_ml[qi * 2 + 1] = l;
+      }
+    }
+  }
+}
+
+// Block attention + merge: CTA = (32 query vectors of one branch and KV head,
+// two warps).  Query vector v is block position n = v / G with query head
+// kvh * G + v % G; its query is the one of the row's resolved source; its
+// block keys/values are the branch's own table K_i[m] = QKV[rcslot(i, m)].
+constexpr int kBQT = 32;
+
+template <int HD>
+__global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int LD = HD + 8;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int slot[kKB];
+  bf16* sQ = reinterpret_cast<bf16*>(smem);
+  bf16* sK = sQ + kBQT * LD;
+  bf16* sV = sK + kKB * LD;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rb = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;  // rb = r * Bp + i
+  const int G = a.nq / a.nkv, L = a.L;
+  const int q0 = blockIdx.x * kBQT, nqv = L * G;
+  if (q0 >= nqv) return;
+  const int count = a.meta[0];
+  const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
+  const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
+  for (int m = tid; m < kKB; m += 64) {
+    int g = m < L ? a.rcslot[rb * L + m] : 0;
+    if (g < 0 || g >= count) {
+      raise_error(a.err, kErrAttn);
+      g = 0;
+    }
+    slot[m] = g;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < kBQT * (HD / 8); idx += 64) {
+    const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (v < nqv)
+      val = *reinterpret_cast<const uint4*>(qkv + (size_t)slot[v / G] * a.ld_qkv + (kvh * G + v % G) * HD + c8 * 8);
+    *reinterpret_cast<uint4*>(sQ + row * LD + c8 * 8) = val;
+  }
+  for (int idx = tid; idx < kKB * (HD / 8); idx += 64) {
+    const int m = idx / (HD / 8), c8 = idx % (HD / 8);
+    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+    if (m < L) {
+      const bf16* src = qkv + (size_t)slot[m] * a.ld_qkv;
+      kv = *reinterpret_cast<const uint4*>(src + koff + c8 * 8);
+      vv = *reinterpret_cast<const uint4*>(src + voff + c8 * 8);
+    }
+    *reinterpret_cast<uint4*>(sK + m * LD + c8 * 8) = kv;
+    *reinterpret_cast<uint4*>(sV + m * LD + c8 * 8) = vv;
+  }
+  __syncthreads();
+  uint32_t qf[HD / 16][4];
+  load_q_frags<HD>(qf, sQ, warp, lane);
+  float sc[kKB / 8][4];
+  qk_scores<HD>(sc, qf, sK, lane);
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < kKB / 8; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int m = nt * 8 + (lane & 3) * 2 + (e & 1);
+      sc[nt][e] = m < L ? sc[nt][e] * a.scale_log2 : -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+  }
+  const float mb0 = quad_max(mx0), mb1 = quad_max(mx1);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < kKB / 8; ++nt) {
+    sc[nt][0] = exp2f(sc[nt][0] - mb0);
+    sc[nt][1] = exp2f(sc[nt][1] - mb0);
+    sc[nt][2] = exp2f(sc[nt][2] - mb1);
+    sc[nt][3] = exp2f(sc[nt][3] - mb1);
+    s0 += sc[nt][0] + sc[nt][1];
+    s1 += sc[nt][2] + sc[nt][3];
+  }
+  const float lb0 = quad_sum(s0), lb1 = quad_sum(s1);
+  float o[HD / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  pv_accum<HD>(o, sc, sV, lane);
+
+  bf16* out = reinterpret_cast<bf16*>(a.attn);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
+    if (v >= nqv) continue;
+    const int row = rb * L + v / G, h = kvh * G + v % G;
+    const int g = slot[v / G];
+    const float mb = half ? mb1 : mb0, lb = half ? lb1 : lb0;
+    float acc[HD / 8][2];
+    float l, wb;
+    if (a.P > 0) {
+      // the merged prefix state of this query (one per recompute slot and head)
+      const size_t qi = (size_t)g * a.nq + h;
+      const float mp = a.part_ml[qi * 2], lp = a.part_ml[qi * 2 + 1];
+      float2 pp[HD / 8];
+      const float* po = a.part_o + qi * HD + (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < HD / 8; ++nt) pp[nt] = *reinterpret_cast<const float2*>(po + nt * 8);
+      const float M = fmaxf(mb, mp);
+      wb = exp2f(mb - M);
+      const float wp = exp2f(mp - M);
+      l = lb * wb + lp * wp;
+#pragma unroll
+      for (int nt = 0; nt < HD / 8; ++nt) {
+        acc[nt][0] = o[nt][2 * half] * wb + wp * pp[nt].x;
+        acc[nt][1] = o[nt][2 * half + 1] * wb + wp * pp[nt].y;
+      }
+    } else {
+      l = lb;
+#pragma unroll
+      for (int nt = 0; nt < HD / 8; ++nt) {
+        acc[nt][0] = o[nt][2 * half];
+        acc[nt][1] = o[nt][2 * half + 1];
+      }
+    }
+    const float inv = 1.f / l;
+    bf16* dst = out + (size_t)row * a.ld_attn + h * HD + (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < HD / 8; ++nt)
+      *reinterpret_cast<__nv_bfloat162*>(dst + nt * 8) = __floats2bfloat162_rn(acc[nt][0] * inv, acc[nt][1] * inv);
+  }
+}
+
+// ------------------------------------------------------------ CUDA-core path (fp32 contexts)
 
 template <typename TAct>
-__global__ void __launch_bounds__(128) attn_prefix_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(128) attn_prefix_simt(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float qs[4][kMaxHd];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qv = blockIdx.x * 4 + warp;
   const int g = qv / a.nq, h = qv % a.nq;
+  const Splits sp = prefix_splits(a);
+  const int s = blockIdx.y;
+  if (s >= sp.S) return;
   const int count = a.meta[0];
   if (g >= count) return;
   int r = 0;
@@ -35,8 +498,7 @@ __global__ void __launch_bounds__(128) attn_prefix_kernel(const AttnArgs a) {
   const TAct* qkv = reinterpret_cast<const TAct*>(a.qkv);
   for (int j = lane; j < hd; j += 32) qs[warp][j] = to_f32<TAct>(qkv[(size_t)g * a.ld_qkv + h * hd + j]);
   __syncwarp();
-  const int s = blockIdx.y;
-  const int k_lo = s * a.split_len, k_hi = min(a.P, k_lo + a.split_len);
+  const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
   const TAct* K = reinterpret_cast<const TAct*>(a.pk) + (size_t)r * a.P * a.nkv * hd + kvh * hd;
   const TAct* V = reinterpret_cast<const TAct*>(a.pv) + (size_t)r * a.P * a.nkv * hd + kvh * hd;
   const size_t kstride = (size_t)a.nkv * hd;
@@ -75,7 +537,9 @@ __global__ void __launch_bounds__(128) attn_prefix_kernel(const AttnArgs a) {
 }
 
 template <typename TAct>
-__global__ void __launch_bounds__(128) attn_block_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(128) attn_block_simt(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float qs[4][kMaxHd];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int w = blockIdx.x * 4 + warp;
@@ -91,9 +555,8 @@ __global__ void __launch_bounds__(128) attn_block_kernel(const AttnArgs a) {
   const TAct* qkv = reinterpret_cast<const TAct*>(a.qkv);
   for (int j = lane; j < hd; j += 32) qs[warp][j] = to_f32<TAct>(qkv[(size_t)g * a.ld_qkv + h * hd + j]);
   __syncwarp();
-  const int base = (row / L) * L;  // first row of this branch
+  const int base = (row / L) * L;
   const int koff = (a.nq + kvh) * hd, voff = (a.nq + a.nkv + kvh) * hd;
-  // block scores, one key per lane per round (L <= 64)
   float sc[2] = {-INFINITY, -INFINITY};
   int ks[2] = {0, 0};
   for (int rr = 0; rr < 2; ++rr) {
@@ -110,14 +573,14 @@ __global__ void __launch_bounds__(128) attn_block_kernel(const AttnArgs a) {
       sc[rr] = dot * a.scale_log2;
     }
   }
+  const Splits sp = prefix_splits(a);
   float M = warp_max(fmaxf(sc[0], sc[1]));
-  for (int s = 0; s < a.n_splits; ++s) M = fmaxf(M, a.part_ml[(((size_t)s * a.T + g) * a.nq + h) * 2]);
+  for (int s = 0; s < sp.S; ++s) M = fmaxf(M, a.part_ml[(((size_t)s * a.T + g) * a.nq + h) * 2]);
   float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < a.n_splits; ++s) {
+  for (int s = 0; s < sp.S; ++s) {
     const size_t qi = ((size_t)s * a.T + g) * a.nq + h;
-    const float ms = a.part_ml[qi * 2], ls = a.part_ml[qi * 2 + 1];
-    const float wgt = exp2f(ms - M);  // 0 for an empty split (ms = -inf)
-    l += wgt * ls;
+    const float wgt = exp2f(a.part_ml[qi * 2] - M);
+    l += wgt * a.part_ml[qi * 2 + 1];
     for (int c = 0; c < per; ++c) acc[c] += wgt * a.part_o[qi * hd + lane + 32 * c];
   }
   float p[2];
@@ -137,16 +600,45 @@ __global__ void __launch_bounds__(128) attn_block_kernel(const AttnArgs a) {
   for (int c = 0; c < per; ++c) out[lane + 32 * c] = from_f32<TAct>(acc[c] * inv);
 }
 
-template <typename TAct>
-cudaError_t attention_impl(Launch& lc, const AttnArgs& a) {
-  if (a.P > 0 && a.n_splits > 0) {
-    dim3 grid((a.T * a.nq + 3) / 4, a.n_splits);
+template <int HD>
+cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
+  constexpr int LD = HD + 8;
+  const int G = a.nq / a.nkv;
+  const size_t smem_p = (size_t)(kQT + 4 * kKB) * LD * sizeof(bf16);
+  const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16);
+  static cudaError_t attr = [&] {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((kQT + 4 * kKB) * LD * sizeof(bf16)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_block_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
+    return e;
+  }();
+  if (attr != cudaSuccess) return lc.err = attr;
+  if (a.P > 0) {
+    // worst case: every row of a request recomputes
+    dim3 grid((a.Bp * a.L * G + kQT - 1) / kQT, a.R * a.nkv, kMaxSplits);
     lc.before(SF_K_ATTN_PREFIX);
-    attn_prefix_kernel<TAct><<<grid, 128, 0, lc.st>>>(a);
+    lc.check(launch_pdl(lc.st, grid, dim3(128), smem_p, kMaxSplits, attn_prefix_mma<HD>, a));
+    lc.after(SF_K_ATTN_PREFIX);
+  }
+  dim3 grid((a.L * G + kBQT - 1) / kBQT, a.R * a.Bp * a.nkv);
+  lc.before(SF_K_ATTN_BLOCK);
+  lc.check(launch_pdl(lc.st, grid, dim3(64), smem_b, 1, attn_block_mma<HD>, a));
+  lc.after(SF_K_ATTN_BLOCK);
+  return lc.err;
+}
+
+template <typename TAct>
+cudaError_t attention_simt(Launch& lc, const AttnArgs& a) {
+  if (a.P > 0) {
+    dim3 grid((a.T * a.nq + 3) / 4, kMaxSplits);
+    lc.before(SF_K_ATTN_PREFIX);
+    lc.check(launch_pdl(lc.st, grid, dim3(128), 0, 1, attn_prefix_simt<TAct>, a));
     lc.after(SF_K_ATTN_PREFIX);
   }
   lc.before(SF_K_ATTN_BLOCK);
-  attn_block_kernel<TAct><<<(a.T * a.nq + 3) / 4, 128, 0, lc.st>>>(a);
+  lc.check(launch_pdl(lc.st, dim3((a.T * a.nq + 3) / 4), dim3(128), 0, 1, attn_block_simt<TAct>, a));
   lc.after(SF_K_ATTN_BLOCK);
   return lc.err;
 }
@@ -154,9 +646,11 @@ cudaError_t attention_impl(Launch& lc, const AttnArgs& a) {
 }  // namespace
 
 cudaError_t launch_attention(Launch& lc, int act_bf16, const AttnArgs& a) {
-  if (a.hd > kMaxHd || a.hd % 32 != 0 || a.L > 64) return cudaErrorInvalidValue;
-  if (act_bf16) return attention_impl<__nv_bfloat16>(lc, a);
-  return attention_impl<float>(lc, a);
+  if (a.hd > kMaxHd || a.hd % 32 != 0 || a.L > kKB) return cudaErrorInvalidValue;
+  if (!act_bf16) return attention_simt<float>(lc, a);
+  if (a.hd == 128) return attention_mma<128>(lc, a);
+  if (a.hd == 64) return attention_mma<64>(lc, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace sf

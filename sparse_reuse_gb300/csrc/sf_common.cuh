@@ -107,3 +107,38 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 
 }  // namespace sf
+
+namespace sf {
+
+// Programmatic dependent launch.  Every kernel of the pass is launched with
+// programmatic stream serialisation: it may start while the previous kernel
+// drains, runs its prologue, and calls pdl_wait() before its first read of
+// anything an earlier kernel wrote (and before it can complete).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(cudaStream_t st, dim3 grid, dim3 block, size_t smem, int cluster_z, Kernel kernel,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_z > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = (unsigned)cluster_z;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace sf

@@ -3,6 +3,10 @@
 // fp32 accumulators of features m0 + l + 32c, c = 0..3, so the rotary pair
 // (j, j + hd/2) of a head and the gate/up pair of a SwiGLU tile sit in the
 // same thread for hd in {64, 128}.
+//
+// prefetch() issues the row's global reads (residual input, rotary table)
+// and apply() consumes them, so a warp can start the reads of several rows
+// before it waits on any of them.
 #pragma once
 
 #include "sf_common.cuh"
@@ -26,22 +30,46 @@ struct EpiQKV {
     int P;
     const float2* rope;  // [pos][hd/2] (cos, sin)
   };
-  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4]) {
+  struct Pre {
+    float2 cs[4];
+  };
+  static __device__ __forceinline__ void prefetch(const Params& p, int g, int m0, int lane, Pre& pre) {
     const int pos = p.P + (p.rc[g] % p.L);
     const int half = p.hd >> 1;
+    // m0 is a multiple of 128 and hd divides 128, so j % half = (lane + 32c) % half
+    const float2* row = p.rope + (size_t)pos * half;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int f = m0 + lane + 32 * c;
+      pre.cs[c] = f < p.qk_dim ? row[(lane + 32 * c) & (half - 1)] : make_float2(1.f, 0.f);
+    }
+  }
+  // hd = 128: a tile is one head, feature l + 32c pairs with l + 32(c ^ 2);
+  // hd = 64: a tile is two heads, the pair is l + 32(c ^ 1).  The partner is a
+  // compile-time index in both cases, so v stays in registers.
+  template <int PAIR>
+  static __device__ __forceinline__ void rotate_store(const Params& p, int g, int m0, int lane, const float v[4],
+                                                      const Pre& pre) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int f = m0 + lane + 32 * c;
       if (f >= p.M) continue;
       float o = v[c];
       if (f < p.qk_dim) {
-        const int j = f % p.hd;
-        const int pc = (p.hd == 128) ? (c ^ 2) : (c ^ 1);
-        const float2 cs = p.rope[(size_t)pos * half + (j % half)];
-        o = (j < half) ? (v[c] * cs.x - v[pc] * cs.y) : (v[c] * cs.x + v[pc] * cs.y);
+        const float2 cs = pre.cs[c];
+        const float w = v[c ^ PAIR];
+        // the first half of each head subtracts the partner, the second adds it
+        o = ((c & PAIR) == 0) ? (v[c] * cs.x - w * cs.y) : (v[c] * cs.x + w * cs.y);
       }
       p.qkv[(size_t)g * p.ld + f] = from_f32<TAct>(o);
     }
+  }
+  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
+                                               const Pre& pre) {
+    if (p.hd == 128)
+      rotate_store<2>(p, g, m0, lane, v, pre);
+    else
+      rotate_store<1>(p, g, m0, lane, v, pre);
   }
 };
 
@@ -53,12 +81,17 @@ struct EpiResidual {
     const float* H;
     int ld;
   };
-  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4]) {
+  struct Pre {
+    float H[4];
+  };
+  static __device__ __forceinline__ void prefetch(const Params& p, int g, int m0, int lane, Pre& pre) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const size_t o = (size_t)g * p.ld + m0 + lane + 32 * c;
-      p.h[o] = p.H[o] + v[c];
-    }
+    for (int c = 0; c < 4; ++c) pre.H[c] = p.H[(size_t)g * p.ld + m0 + lane + 32 * c];
+  }
+  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
+                                               const Pre& pre) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) p.h[(size_t)g * p.ld + m0 + lane + 32 * c] = pre.H[c] + v[c];
   }
 };
 
@@ -70,7 +103,10 @@ struct EpiSwiGLU {
     TAct* u;
     int ld;
   };
-  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4]) {
+  struct Pre {};
+  static __device__ __forceinline__ void prefetch(const Params&, int, int, int, Pre&) {}
+  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
+                                               const Pre&) {
     const int t = m0 >> 7;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -87,10 +123,37 @@ struct EpiStore {
     float* y;
     int ld;
   };
-  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4]) {
+  struct Pre {};
+  static __device__ __forceinline__ void prefetch(const Params&, int, int, int, Pre&) {}
+  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
+                                               const Pre&) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) p.y[(size_t)g * p.ld + m0 + lane + 32 * c] = v[c];
   }
 };
+
+// Epilogue of the 32-row chunk starting at row0 for the rows jj = ew + 4b
+// (b = 0..7, jj < nvalid) handled by epilogue warp ew: the global reads of all
+// eight rows are issued before any is consumed.  getv(jj, v) supplies the
+// fp32 accumulators of row jj for this lane's four features.
+template <class Epi, class GetV>
+__device__ __forceinline__ void epilogue_chunk(const typename Epi::Params& ep, int row0, int nvalid, int m0,
+                                               int ew, int lane, GetV getv) {
+  typename Epi::Pre pre[8];
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const int jj = ew + 4 * b;
+    if (jj < nvalid) Epi::prefetch(ep, row0 + jj, m0, lane, pre[b]);
+  }
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const int jj = ew + 4 * b;
+    if (jj < nvalid) {
+      float vv[4];
+      getv(jj, vv);
+      Epi::apply(ep, row0 + jj, m0, lane, vv, pre[b]);
+    }
+  }
+}
 
 }  // namespace sf

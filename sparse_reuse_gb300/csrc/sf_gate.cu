@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
   __shared__ int tmp[32];
   __shared__ bool is_last;
   extern __shared__ __align__(16) unsigned char dyn[];
+  pdl_wait();
+  pdl_trigger();
 
   const int row = blockIdx.x;
   const int L = a.L, Bp = a.tree.Bp;
@@ -165,6 +167,8 @@ __global__ void __launch_bounds__(256) rmsnorm_gather_kernel(const float* X, con
                                                              int max_rows, const float* gain, float eps, TAct* out,
                                                              int d, unsigned* err) {
   __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
   const int count = count_ptr ? *count_ptr : max_rows;
   const int d4 = d >> 2;
   for (int g = blockIdx.x; g < count; g += gridDim.x) {
@@ -194,6 +198,8 @@ __global__ void __launch_bounds__(256) rmsnorm_gather_kernel(const float* X, con
 template <typename TOut>
 __global__ void __launch_bounds__(256) final_residual_kernel(const float* h, const float* f, const int32_t* rcslot,
                                                              TOut* out, float* dbg, int T, int d, unsigned* err) {
+  pdl_wait();
+  pdl_trigger();
   const int d4 = d >> 2;
   for (int row = blockIdx.x; row < T; row += gridDim.x) {
     int s = rcslot[row];
@@ -244,11 +250,11 @@ cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16) {
   const size_t dyn = ((a.T + 15) & ~15) + (size_t)a.T * sizeof(int);
   lc.before(SF_K_GATE);
   if (a.x_in == nullptr)
-    gate_kernel<false, float><<<a.T, kGateThreads, dyn, lc.st>>>(a);
+    lc.check(launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, gate_kernel<false, float>, a));
   else if (in_bf16)
-    gate_kernel<true, __nv_bfloat16><<<a.T, kGateThreads, dyn, lc.st>>>(a);
+    lc.check(launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, gate_kernel<true, __nv_bfloat16>, a));
   else
-    gate_kernel<true, float><<<a.T, kGateThreads, dyn, lc.st>>>(a);
+    lc.check(launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, gate_kernel<true, float>, a));
   lc.after(SF_K_GATE);
   return lc.err;
 }
@@ -259,10 +265,11 @@ cudaError_t launch_rmsnorm_gather(Launch& lc, int fam, const float* X, const int
   lc.before(fam);
   const int grid = grid_rows(max_rows);
   if (act_bf16)
-    rmsnorm_gather_kernel<__nv_bfloat16><<<grid, 256, 0, lc.st>>>(X, rc, count, max_rows, gain, eps,
-                                                                   (__nv_bfloat16*)out, d, err);
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, rmsnorm_gather_kernel<__nv_bfloat16>, X, rc, count,
+                        max_rows, gain, eps, (__nv_bfloat16*)out, d, err));
   else
-    rmsnorm_gather_kernel<float><<<grid, 256, 0, lc.st>>>(X, rc, count, max_rows, gain, eps, (float*)out, d, err);
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, rmsnorm_gather_kernel<float>, X, rc, count, max_rows,
+                        gain, eps, (float*)out, d, err));
   lc.after(fam);
   return lc.err;
 }
@@ -272,9 +279,11 @@ cudaError_t launch_final_residual(Launch& lc, const float* h, const float* f, co
   lc.before(SF_K_RESIDUAL);
   const int grid = grid_rows(T);
   if (out_bf16)
-    final_residual_kernel<__nv_bfloat16><<<grid, 256, 0, lc.st>>>(h, f, rcslot, (__nv_bfloat16*)out, dbg, T, d, err);
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, final_residual_kernel<__nv_bfloat16>, h, f, rcslot,
+                        (__nv_bfloat16*)out, dbg, T, d, err));
   else
-    final_residual_kernel<float><<<grid, 256, 0, lc.st>>>(h, f, rcslot, (float*)out, dbg, T, d, err);
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, final_residual_kernel<float>, h, f, rcslot, (float*)out,
+                        dbg, T, d, err));
   lc.after(SF_K_RESIDUAL);
   return lc.err;
 }

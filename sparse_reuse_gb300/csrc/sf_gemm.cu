@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TAct* __restrict__
                                                         const int32_t* count_ptr, int dense_count, int K) {
   __shared__ float As[kBK][kBM + 4];
   __shared__ float Bs[kBK][kBN + 4];
+  pdl_wait();
+  pdl_trigger();
   const int count = count_ptr ? *count_ptr : dense_count;
   const int g0 = blockIdx.y * kBM, o0 = blockIdx.x * kBN;
   if (g0 >= count) return;
@@ -67,6 +69,8 @@ template <class Epi>
 __global__ void __launch_bounds__(128) epilogue_kernel(const float* __restrict__ Y, int ldy, int n_tiles,
                                                       const int32_t* count_ptr, int dense_count,
                                                       const typename Epi::Params p) {
+  pdl_wait();
+  pdl_trigger();
   const int count = count_ptr ? *count_ptr : dense_count;
   const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int g = w / n_tiles, t = w % n_tiles;
@@ -74,7 +78,9 @@ __global__ void __launch_bounds__(128) epilogue_kernel(const float* __restrict__
   float v[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) v[c] = Y[(size_t)g * ldy + t * 128 + lane + 32 * c];
-  Epi::apply(p, g, t * 128, lane, v);
+  typename Epi::Pre pre;
+  Epi::prefetch(p, g, t * 128, lane, pre);
+  Epi::apply(p, g, t * 128, lane, v, pre);
 }
 
 template <typename TAct>
@@ -82,8 +88,8 @@ cudaError_t gemm_simt(Launch& lc, int fam, const GemmArgs& g, EpiKind kind, cons
   const int ldy = g.M;
   dim3 grid(g.M / kBN, (g.max_rows + kBM - 1) / kBM);
   lc.before(fam);
-  gemm_simt_kernel<TAct><<<grid, 256, 0, lc.st>>>((const TAct*)g.X, g.ldx, (const TAct*)g.W, g.ldw, y32, ldy,
-                                                  g.count, g.dense_count, g.K);
+  lc.check(launch_pdl(lc.st, grid, dim3(256), 0, 1, gemm_simt_kernel<TAct>, (const TAct*)g.X, g.ldx,
+                      (const TAct*)g.W, g.ldw, y32, ldy, g.count, g.dense_count, g.K));
   lc.after(fam);
   const int n_tiles = g.M / 128;
   const int blocks = (g.max_rows * n_tiles + 3) / 4;
@@ -91,22 +97,22 @@ cudaError_t gemm_simt(Launch& lc, int fam, const GemmArgs& g, EpiKind kind, cons
   switch (kind) {
     case kEpiQKV: {
       typename EpiQKV<TAct>::Params p{(TAct*)e.qkv, e.qkv_ld, e.qk_dim, e.qkv_M, e.hd, e.rc, e.L, e.P, e.rope};
-      epilogue_kernel<EpiQKV<TAct>><<<blocks, 128, 0, lc.st>>>(y32, ldy, n_tiles, g.count, g.dense_count, p);
+      lc.check(launch_pdl(lc.st, dim3(blocks), dim3(128), 0, 1, epilogue_kernel<EpiQKV<TAct>>, (const float*)y32, ldy, n_tiles, g.count, g.dense_count, p));
       break;
     }
     case kEpiResidual: {
       EpiResidual::Params p{e.h, e.H, e.h_ld};
-      epilogue_kernel<EpiResidual><<<blocks, 128, 0, lc.st>>>(y32, ldy, n_tiles, g.count, g.dense_count, p);
+      lc.check(launch_pdl(lc.st, dim3(blocks), dim3(128), 0, 1, epilogue_kernel<EpiResidual>, (const float*)y32, ldy, n_tiles, g.count, g.dense_count, p));
       break;
     }
     case kEpiSwiGLU: {
       typename EpiSwiGLU<TAct>::Params p{(TAct*)e.u, e.u_ld};
-      epilogue_kernel<EpiSwiGLU<TAct>><<<blocks, 128, 0, lc.st>>>(y32, ldy, n_tiles, g.count, g.dense_count, p);
+      lc.check(launch_pdl(lc.st, dim3(blocks), dim3(128), 0, 1, epilogue_kernel<EpiSwiGLU<TAct>>, (const float*)y32, ldy, n_tiles, g.count, g.dense_count, p));
       break;
     }
     case kEpiStore: {
       EpiStore::Params p{e.y, e.y_ld};
-      epilogue_kernel<EpiStore><<<blocks, 128, 0, lc.st>>>(y32, ldy, n_tiles, g.count, g.dense_count, p);
+      lc.check(launch_pdl(lc.st, dim3(blocks), dim3(128), 0, 1, epilogue_kernel<EpiStore>, (const float*)y32, ldy, n_tiles, g.count, g.dense_count, p));
       break;
     }
   }

@@ -69,19 +69,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int count = p.count ? *p.count : p.dense_count;
   const int m_tile = blockIdx.x, n_tile = blockIdx.y;
   const int S = p.splits;
   const int z = S > 1 ? (int)cluster_ctarank() : 0;
   const int row0 = n_tile * BN;
-  if (row0 >= count) return;  // uniform over the cluster (same n_tile)
-  const int n_rows = min(BN, count - row0);
-  const int n_mma = (n_rows + 15) & ~15;
-  const int n_chunks = (n_rows + RC - 1) / RC;
   const int nk = p.K / BK;
   const int kb0 = (int)((long long)z * nk / S);
   const int kb1 = (int)((long long)(z + 1) * nk / S);
   const int m0 = m_tile * BM;
+  // The first row tile always has rows unless the count is zero; later row
+  // tiles learn from the live count whether they have work before they
+  // allocate anything (the decision is uniform over a cluster).
+  const bool lead = n_tile == 0;
+  if (!lead) {
+    pdl_wait();
+    pdl_trigger();
+    const int c0 = p.count ? *p.count : p.dense_count;
+    if (row0 >= c0) return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -96,6 +101,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // weight tiles of the first stages do not depend on earlier kernels: start
+  // streaming them before waiting for the kernel that produced the rows
+  const int npre = lead ? min(STAGES, kb1 - kb0) : 0;
+  if (warp == 0 && lane == 0) {
+    for (int it = 0; it < npre; ++it) {
+      mbar_expect_tx_only(&full[it], A_BYTES);
+      tma_load_2d(sA + it * A_BYTES, &tmA, (kb0 + it) * BK, m0, &full[it]);
+    }
+  }
+  if (lead) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  const int count = p.count ? *p.count : p.dense_count;
+  const bool active = row0 < count;  // uniform over the cluster
+  const int n_rows = active ? min(BN, count - row0) : 0;
+  const int n_mma = (n_rows + 15) & ~15;
+  const int n_chunks = (n_rows + RC - 1) / RC;
   const int q = warp & 3;
   const int f = q * 32 + lane;
   const int ew = warp - 2;
@@ -105,21 +128,33 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       int it = 0;
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, p.err)) break;
-        mbar_expect_tx(&full[s], A_BYTES + n_chunks * B_CHUNK);
-        tma_load_2d(sA + s * A_BYTES, &tmA, kb * BK, m0, &full[s]);
-        for (int c = 0; c < n_chunks; ++c)
-          tma_load_2d(sB + s * B_BYTES + c * B_CHUNK, &tmB, kb * BK, row0 + c * RC, &full[s]);
+      if (!active) {
+        // no rows: let the prefetched weight tiles land before leaving
+        for (; it < npre; ++it) {
+          mbar_arrive(&full[it]);
+          mbar_wait(&full[it], 0, p.err);
+        }
+      } else {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (it < npre) {
+            mbar_expect_tx(&full[s], n_chunks * B_CHUNK);
+          } else {
+            if (!mbar_wait(&empty[s], ph ^ 1, p.err)) break;
+            mbar_expect_tx(&full[s], A_BYTES + n_chunks * B_CHUNK);
+            tma_load_2d(sA + s * A_BYTES, &tmA, kb * BK, m0, &full[s]);
+          }
+          for (int c = 0; c < n_chunks; ++c)
+            tma_load_2d(sB + s * B_BYTES + c * B_CHUNK, &tmB, kb * BK, row0 + c * RC, &full[s]);
+        }
+        // every copy this CTA issued lands before its shared memory is reused
+        for (int j = max(0, it - STAGES); j < it; ++j) mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.err);
       }
-      // every copy this CTA issued lands before its shared memory is reused
-      for (int j = max(0, it - STAGES); j < it; ++j) mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && active) {
       const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
       int it = 0;
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -139,7 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(tfull, 0, p.err);
     }
     __syncwarp();
-  } else {
+  } else if (active) {
     go = mbar_wait(tfull, 0, p.err);
     fence_after_sync();
     if (S == 1 && go) {
@@ -150,18 +185,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) stage[j * STAGE_LD + f] = v[j];
         named_bar_sync(1, 128);
-        for (int jj = ew; jj < 32 && j0 + jj < n_rows; jj += 4) {
-          float vv[4];
+        epilogue_chunk<Epi>(ep, row0 + j0, min(32, n_rows - j0), m0, ew, lane, [&](int jj, float (&vv)[4]) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) vv[c] = stage[jj * STAGE_LD + lane + 32 * c];
-          Epi::apply(ep, row0 + j0 + jj, m0, lane, vv);
-        }
+        });
         named_bar_sync(1, 128);
       }
     }
   }
 
-  if (S > 1) {
+  if (S > 1 && active) {
     // chunk c (32 rows) belongs to cluster rank c % S, which keeps the
     // partials of every rank for it at buf[rank][c / S][row][feature]
     const int nc = (n_rows + 31) / 32;
@@ -185,15 +218,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int lc = 0; lc < n_own; ++lc) {
         const int c = z + lc * S;
         if (c >= nc) break;
-        for (int jj = ew; jj < 32 && c * 32 + jj < n_rows; jj += 4) {
-          float vv[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int s = 0; s < S; ++s) {
-            const float* src = buf + ((size_t)(s * n_own + lc) * 32 + jj) * BM + lane;
+        epilogue_chunk<Epi>(ep, row0 + c * 32, min(32, n_rows - c * 32), m0, ew, lane,
+                            [&](int jj, float (&vv)[4]) {
+                              vv[0] = vv[1] = vv[2] = vv[3] = 0.f;
+                              for (int s = 0; s < S; ++s) {
+                                const float* src = buf + ((size_t)(s * n_own + lc) * 32 + jj) * BM + lane;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) vv[cc] += src[32 * cc];
-          }
-          Epi::apply(ep, row0 + c * 32 + jj, m0, lane, vv);
-        }
+                                for (int cc = 0; cc < 4; ++cc) vv[cc] += src[32 * cc];
+                              }
+                            });
       }
     }
   }
@@ -259,11 +292,42 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Largest number of clusters of size s (2..8) that can be resident at once.
+int max_active_clusters(int s) {
+  static int cache[9] = {0};
+  static std::once_flag once;
+  std::call_once(once, [] {
+    set_smem_attr<EpiStore>();
+    for (int c = 2; c <= 8; ++c) {
+      if (!tc::split_fits(c)) continue;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1, 1, c);
+      cfg.blockDim = dim3(tc::THREADS);
+      cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = (unsigned)c;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, tc::gemm_tc_kernel<EpiStore>, &cfg) != cudaSuccess) n = 0;
+      cache[c] = n;
+    }
+    cudaGetLastError();
+  });
+  return (s >= 2 && s <= 8) ? cache[s] : 0;
+}
+
+// K splits for an M x K weight over n_tiles row tiles: the largest cluster
+// size that keeps every (m, n) tile resident in one wave and gives each CTA
+// at least one K block.
 int gemm_tc_splits(int M, int K, int n_tiles) {
-  const int m_tiles = M / tc::BM, nk = K / tc::BK;
-  const int want = std::min(sm_count() / std::max(1, m_tiles * n_tiles), nk);
+  const int m_tiles = M / tc::BM, nk = K / tc::BK, tiles = std::max(1, m_tiles * n_tiles);
+  const int want = std::min(sm_count() / tiles, nk);
   for (int s = 8; s > 1; --s)
-    if (s <= want && tc::split_fits(s)) return s;
+    if (s <= want && tc::split_fits(s) && max_active_clusters(s) >= tiles) return s;
   return 1;
 }
 
@@ -274,19 +338,8 @@ cudaError_t launch_tc(const TcGemm& g, const typename Epi::Params& ep, cudaStrea
   cudaError_t e = set_smem_attr<Epi>();
   if (e != cudaSuccess) return e;
   tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(g.M / tc::BM, (g.max_rows + tc::BN - 1) / tc::BN, g.splits);
-  cfg.blockDim = dim3(tc::THREADS);
-  cfg.dynamicSmemBytes = tc::SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = (unsigned)g.splits;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p, ep);
+  return launch_pdl(st, dim3(g.M / tc::BM, (g.max_rows + tc::BN - 1) / tc::BN, g.splits), dim3(tc::THREADS),
+                    tc::SMEM_BYTES, g.splits, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p, ep);
 }
 
 }  // namespace

@@ -50,6 +50,7 @@ struct sf_ctx {
   int act_bytes = 4;
   int q_dim = 0, kv_dim = 0, Mqkv = 0, Mqkv_pad = 0, Fp = 0, Mgu = 0;
   int T_max = 0, max_pos = 0;
+  int sm_count = 148;
   std::vector<sf_layer_dev> layers;
 
   // workspaces (device)
@@ -92,6 +93,7 @@ struct sf_ctx {
   cudaGraphExec_t graph_exec = nullptr;
   uint64_t graph_nodes = 0;
   uint64_t graph_family[SF_K_COUNT] = {};
+  cudaGraphExec_t timing_exec = nullptr;  // last timed pass (kept until its events are read)
 };
 
 namespace sf {
@@ -102,10 +104,14 @@ struct Launch {
   sf_ctx* ctx;
   cudaStream_t st;
   cudaError_t err = cudaSuccess;
+  bool external_events = false;  // recording into a graph under capture
   uint64_t launches = 0;
   uint64_t family[SF_K_COUNT] = {};
   void before(int fam);
   void after(int fam);
+  void check(cudaError_t e) {
+    if (e != cudaSuccess && err == cudaSuccess) err = e;
+  }
 };
 
 struct GemmArgs {
@@ -193,7 +199,7 @@ struct AttnArgs {
   float* part_o; float* part_ml;
   void* attn; int ld_attn;
   int R, Bp, L, P, T, nq, nkv, hd;
-  int n_splits, split_len;
+  int target_ctas;  // prefix splits are chosen on the device to reach about this many CTAs
   float scale_log2;
   unsigned* err;
 };

@@ -108,6 +108,26 @@ def test_bf16_small_free_running_dense_and_folded():
             check_free_running(cfg, wl, gpu, delta)
 
 
+BF16_CASES = {
+    "hd64_ragged": dict(head_dim=64, n_q_heads=8, n_kv_heads=2, block_len=20, prefix_len=70, n_drafts=5),
+    "no_prefix": dict(prefix_len=0, n_drafts=3),
+    "three_requests_gqa7": dict(n_requests=3, n_q_heads=7, n_kv_heads=1, prefix_len=200, n_drafts=4),
+    "long_prefix": dict(prefix_len=1000, n_drafts=2, block_len=64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BF16_CASES))
+def test_bf16_variants_teacher_forced(name):
+    base = dict(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=128, d_ffn=320, dtype="bf16",
+                block_len=32, prefix_len=96, n_drafts=4)
+    base.update(BF16_CASES[name])
+    cfg = synth.small_config(**base)
+    wl = _wl(cfg, seed=7)
+    for delta in (0.0, 0.1):
+        gpu = run_gpu(cfg, wl, delta)
+        check_teacher_forced(cfg, wl, gpu, delta, range(cfg.n_layers))
+
+
 def test_1p5b_all_layers_teacher_forced():
     cfg = synth.CONFIGS["1.5b"]
     wl = _wl(cfg)
