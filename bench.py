@@ -162,6 +162,63 @@ def oracle_sample(cfg, wl, delta, budget_s=12.0):
                       f"time per layer x {cfg.n_layers}", "passes_per_s": 1.0 / per_pass}
 
 
+# ------------------------------------------------------------------ config sweep
+
+def sweep(args, dev):
+    """Folded vs dense throughput for every workload config on this GPU."""
+    import torch
+    import synth
+    import sparse_reuse_gb300 as sf
+    pk = peaks()
+    runs = [("tiny", None, [synth.CONFIGS["tiny"].delta]), ("1.5b", None, [0.1]), ("7b", None, [0.1]),
+            ("8b", None, list(synth.DELTA_SWEEP_8B))] + [("14b", b, [0.1]) for b in synth.DRAFT_SWEEP_14B]
+    for name, drafts, deltas in runs:
+        cfg = synth.CONFIGS[name] if drafts is None else synth.CONFIGS[name].with_(n_drafts=drafts)
+        wl = synth.make_workload(cfg, seed=0, device=dev)
+        ctx = sf.from_config(cfg, wl.weights)
+        stream = torch.cuda.Stream(device=dev)
+        nl = cfg.n_layers
+        out = torch.empty_like(wl.hidden)
+        fold = torch.empty((nl, cfg.n_requests, cfg.n_branches, cfg.block_len), dtype=torch.uint8, device=dev)
+        rcc = torch.empty((nl,), dtype=torch.int32, device=dev)
+        pk_ = wl.prefix_k if cfg.prefix_len else None
+        pv_ = wl.prefix_v if cfg.prefix_len else None
+
+        def timed(dl):
+            for _ in range(args.warmup):
+                ctx.verify(wl.hidden, wl.parents, pk_, pv_, dl, out=out, fold=fold, rc_count=rcc, stream=stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                ctx.verify(wl.hidden, wl.parents, pk_, pv_, dl, out=out, fold=fold, rc_count=rcc, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / args.steps
+
+        dense_ms = timed(0.0)
+        dense_rc = rcc.cpu().numpy().tolist()
+        for dl in deltas:
+            ms = timed(dl)
+            rc = rcc.cpu().numpy().tolist()
+            pw = pass_work(cfg, rc)
+            t_roof = max(pw["flops"] / (pk["bf16_tflops"] * 1e12), pw["bytes"] / (pk["hbm_gbs"] * 1e9))
+            pwd = pass_work(cfg, dense_rc)
+            t_roof_d = max(pwd["flops"] / (pk["bf16_tflops"] * 1e12), pwd["bytes"] / (pk["hbm_gbs"] * 1e9))
+            line = {"metric": METRIC, "config": workload_desc(cfg), "delta": dl, "dtype": cfg.dtype,
+                    "ms_per_pass": ms, "passes_per_s": 1e3 / ms, "branch_tokens_per_s": cfg.rows * 1e3 / ms,
+                    "fold_fraction": float(fold[:, :, 1:].float().mean().item()) if cfg.n_drafts else 0.0,
+                    "rc_rows_mean": sum(rc) / len(rc), "pass_roofline_frac": t_roof * 1e3 / ms,
+                    "roofline_bound": "tensor" if pw["flops"] / (pk["bf16_tflops"] * 1e12) >
+                                      pw["bytes"] / (pk["hbm_gbs"] * 1e9) else "hbm",
+                    "dense_ms_per_pass": dense_ms, "dense_branch_tokens_per_s": cfg.rows * 1e3 / dense_ms,
+                    "dense_pass_roofline_frac": t_roof_d * 1e3 / dense_ms, "speedup_vs_dense": dense_ms / ms}
+            print(json.dumps(line), flush=True)
+        ctx.close()
+        del wl, ctx
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -179,6 +236,8 @@ def main():
                     help="profiling only: run the first N layers of the config")
     ap.add_argument("--profile-only", action="store_true",
                     help="profiling only: warm-up and timed passes, nothing else, no JSON line")
+    ap.add_argument("--sweep", action="store_true",
+                    help="every workload config (8B delta sweep, 14B draft sweep): one JSON line each")
     args = ap.parse_args()
 
     import torch
@@ -227,6 +286,10 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import sparse_reuse_gb300 as sf
+
+    if args.sweep:
+        sweep(args, dev)
+        return
 
     wl = synth.make_workload(cfg, seed=rank, device=dev)
     ctx = sf.from_config(cfg, wl.weights)
