@@ -32,10 +32,22 @@ constexpr int kMaxSplits = 8;
 constexpr int kQT = 64;  // query vectors per CTA (16 per warp)
 constexpr int kKB = 64;  // keys per block
 
-// Number of prefix splits and keys per split for this pass (device side).
+// Number of prefix splits and keys per split for this pass.
 struct Splits {
   int S, len;
 };
+
+// Tensor-core path: the split count is fixed on the host from the prefix
+// length alone (at most 512 keys per CTA), so the split CTAs of a query tile
+// form a cluster of exactly that size.
+constexpr int kKeysPerSplit = 512;
+__host__ __device__ __forceinline__ Splits fixed_splits(int P) {
+  if (P <= 0) return {0, 0};
+  int S = (P + kKeysPerSplit - 1) / kKeysPerSplit;
+  S = S < 1 ? 1 : (S > kMaxSplits ? kMaxSplits : S);
+  const int len = (((P + S - 1) / S) + kKB - 1) / kKB * kKB;
+  return {(P + len - 1) / len, len};
+}
 
 __device__ __forceinline__ Splits prefix_splits(const AttnArgs& a) {
   if (a.P <= 0) return {0, 0};
@@ -189,12 +201,12 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const AttnArgs a) {
   float* xbuf = reinterpret_cast<float*>(sK);  // exchange area, reused after the loop
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
-  const Splits sp = prefix_splits(a);
+  const Splits sp = fixed_splits(a.P);
   const int G = a.nq / a.nkv;
   const int off_r = a.meta[1 + r], nqv = (a.meta[2 + r] - off_r) * G;
   const int q0 = blockIdx.x * kQT;
   if (q0 >= nqv) return;  // uniform over the cluster
-  const int s = (int)cluster_rank();
+  const int s = sp.S > 1 ? (int)cluster_rank() : 0;
   const bool has_keys = s < sp.S;
   const int k_lo = s * sp.len, k_hi = has_keys ? min(a.P, k_lo + sp.len) : k_lo;
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
@@ -617,9 +629,10 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   if (attr != cudaSuccess) return lc.err = attr;
   if (a.P > 0) {
     // worst case: every row of a request recomputes
-    dim3 grid((a.Bp * a.L * G + kQT - 1) / kQT, a.R * a.nkv, kMaxSplits);
+    const Splits sp = fixed_splits(a.P);
+    dim3 grid((a.Bp * a.L * G + kQT - 1) / kQT, a.R * a.nkv, sp.S);
     lc.before(SF_K_ATTN_PREFIX);
-    lc.check(launch_pdl(lc.st, grid, dim3(128), smem_p, kMaxSplits, attn_prefix_mma<HD>, a));
+    lc.check(launch_pdl(lc.st, grid, dim3(128), smem_p, sp.S, attn_prefix_mma<HD>, a));
     lc.after(SF_K_ATTN_PREFIX);
   }
   dim3 grid((a.L * G + kBQT - 1) / kBQT, a.R * a.Bp * a.nkv);
