@@ -81,6 +81,29 @@ def pass_work(cfg, rc_counts):
     return tot
 
 
+# ------------------------------------------------------------------ multi-GPU replicas
+
+def replica_seed(rank: int) -> int:
+    """Every rank verifies its own independent requests (weak scaling)."""
+    return rank
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The job's time is the slowest rank's time (no data-path collective)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, rows_per_pass: int, passes: int, seconds: float) -> float:
+    """Branch-tokens per second over all ranks: each rank ran `passes` passes
+    of `rows_per_pass` rows; the job took the slowest rank's `seconds`."""
+    return world * rows_per_pass * passes / seconds
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -291,7 +314,7 @@ def main():
         sweep(args, dev)
         return
 
-    wl = synth.make_workload(cfg, seed=rank, device=dev)
+    wl = synth.make_workload(cfg, seed=replica_seed(rank), device=dev)
     ctx = sf.from_config(cfg, wl.weights)
     stream = torch.cuda.Stream(device=dev)
     nl, T, d = cfg.n_layers, cfg.rows, cfg.d_model
@@ -322,11 +345,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
         return ms, ctx.stats()["kernel_launches"] - s0
 
     if args.profile_only:
@@ -338,12 +357,12 @@ def main():
     rc_fold = rcc.cpu().numpy().tolist()
     fold_frac = float(fold[:, :, 1:].float().mean().item()) if cfg.n_drafts else 0.0
     ms_step = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, T, args.steps, ms / 1e3)
 
     dense = None
     if not args.no_dense:
         dms, _ = timed(0.0, args.steps, args.warmup)
-        dense = {"delta": 0.0, "value": world * T * args.steps / (dms / 1e3), "unit": UNIT,
+        dense = {"delta": 0.0, "value": whole_job_rate(world, T, args.steps, dms / 1e3), "unit": UNIT,
                  "ms_per_step": dms / args.steps, "passes_per_s": world * args.steps / (dms / 1e3),
                  "rc_count": rcc.cpu().numpy().tolist()}
 
@@ -408,11 +427,8 @@ def main():
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
     barrier()
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * T * args.steps / e2e_s, "unit": UNIT,
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
+    e2e = {"value": whole_job_rate(world, T, args.steps, e2e_s), "unit": UNIT,
            "h2d_bytes_per_step": h_host.numel() * h_host.element_size(),
            "d2h_bytes_per_step": o_host.numel() * o_host.element_size() + f_host.numel()}
 
