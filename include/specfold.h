@@ -90,8 +90,9 @@ typedef struct sf_ctx sf_ctx;
  * device memory and allocates every workspace the pass needs for the given
  * capacities (no allocation happens in sf_verify).  Synchronous.
  * Errors: SF_ERR_INVALID_ARG (null), SF_ERR_UNSUPPORTED (head_dim not 64/128,
- * d_model % 128, nq % nkv, block_len > 64, max_requests * max_branches > 1024,
- * more than 8192 rows), SF_ERR_OOM, SF_ERR_CUDA.  *out is NULL on error. */
+ * d_model % 128, nq % nkv, block_len > 64,
+ * max_requests * max_branches > 1024, more than 8192 rows), SF_ERR_OOM,
+ * SF_ERR_CUDA.  *out is NULL on error. */
 sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_ctx** out);
 
 /* Enqueue one verification pass on `stream` (a cudaStream_t; NULL = legacy

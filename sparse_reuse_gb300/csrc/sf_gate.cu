@@ -109,8 +109,13 @@ __device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot
   }
 }
 
-template <bool kLayer0, typename TIn>
-__global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constant__ GateArgs a) {
+// One block per row (r, i, n): the row's layer input H (previous layer's
+// residual applied) and its gate decision against the parent row.  For short
+// rows (VEC > 0) every thread first loads its VEC float4 of the row and of the
+// parent row, then reduces and stores them, so all its loads are in flight at
+// once; long rows (VEC == 0) are streamed in a loop at full occupancy.
+template <bool kLayer0, typename TIn, int VEC>
+__global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ GateArgs a) {
   __shared__ float red[32];
   __shared__ int tmp[32];
   __shared__ bool is_last;
@@ -125,17 +130,45 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
   const int d4 = a.d >> 2;
 
   float diff2 = 0.f, par2 = 0.f;
-  for (int c = threadIdx.x; c < d4; c += blockDim.x) {
-    const float4 x = layer_input4<kLayer0, TIn>(a, row, c);
-    *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
-    if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
-    if (prow >= 0) {
-      // the parent's input is recomputed from the same operands, so it is
-      // bit-identical to what the parent's block writes
-      const float4 y = layer_input4<kLayer0, TIn>(a, prow, c);
-      const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
-      diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
-      par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+  if constexpr (VEC > 0) {
+    float4 xs[VEC], ys[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * blockDim.x;
+      if (c < d4) {
+        xs[k] = layer_input4<kLayer0, TIn>(a, row, c);
+        // the parent's input is recomputed from the same operands, so it is
+        // bit-identical to what the parent's block writes
+        if (prow >= 0) ys[k] = layer_input4<kLayer0, TIn>(a, prow, c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * blockDim.x;
+      if (c < d4) {
+        const float4 x = xs[k];
+        *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
+        if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
+        if (prow >= 0) {
+          const float4 y = ys[k];
+          const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
+          diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
+          par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+        }
+      }
+    }
+  } else {
+    // long rows: stream the row at full occupancy
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+      const float4 x = layer_input4<kLayer0, TIn>(a, row, c);
+      *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
+      if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
+      if (prow >= 0) {
+        const float4 y = layer_input4<kLayer0, TIn>(a, prow, c);
+        const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
+        diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
+        par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+      }
     }
   }
   if (prow >= 0) {
@@ -147,10 +180,10 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
     const uint8_t f = (prow >= 0 && a.delta > 0.f && diff2 <= a.delta * a.delta * par2) ? 1 : 0;
     a.fold[row] = f;
     if (a.fold_user) a.fold_user[row] = f;
+    // only the flag has to be visible before this block's ticket is counted
+    __threadfence();
+    is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!is_last) return;
   __threadfence();
@@ -246,15 +279,29 @@ int grid_rows(int rows) {
 
 }  // namespace
 
+namespace {
+
+template <int VEC>
+cudaError_t launch_gate_vec(Launch& lc, const GateArgs& a, int in_bf16, int threads, size_t dyn) {
+  const dim3 grid(a.T), block(threads);
+  if (a.x_in == nullptr) return launch_pdl(lc.st, grid, block, dyn, 1, gate_kernel<false, float, VEC>, a);
+  if (in_bf16) return launch_pdl(lc.st, grid, block, dyn, 1, gate_kernel<true, __nv_bfloat16, VEC>, a);
+  return launch_pdl(lc.st, grid, block, dyn, 1, gate_kernel<true, float, VEC>, a);
+}
+
+}  // namespace
+
 cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16) {
+  const int d4 = a.d / 4;
+  if (a.d % 4 != 0) return lc.err = cudaErrorInvalidValue;
   const size_t dyn = ((a.T + 15) & ~15) + (size_t)a.T * sizeof(int);
+  // rows of up to 512 float4: 256 threads holding 2 float4 each (and 2 of the
+  // parent); longer rows: the streaming loop
   lc.before(SF_K_GATE);
-  if (a.x_in == nullptr)
-    lc.check(launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, gate_kernel<false, float>, a));
-  else if (in_bf16)
-    lc.check(launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, gate_kernel<true, __nv_bfloat16>, a));
+  if (d4 <= 512)
+    lc.check(launch_gate_vec<2>(lc, a, in_bf16, 256, dyn));
   else
-    lc.check(launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, gate_kernel<true, float>, a));
+    lc.check(launch_gate_vec<0>(lc, a, in_bf16, 256, dyn));
   lc.after(SF_K_GATE);
   return lc.err;
 }
