@@ -23,6 +23,7 @@
 // dimension so every key/value tile is read once per KV head.  FP32 contexts
 // use CUDA-core kernels that keep fp32 operands.
 #include "sf_internal.h"
+#include "sf_tc.cuh"
 
 namespace sf {
 namespace {
@@ -172,6 +173,50 @@ __device__ __forceinline__ void pv_accum(float (&o)[HD / 8][4], const float (&p)
   }
 }
 
+// The same two products with K and V tiles written by TMA: per 64-dim half a
+// [64 keys][128 bytes] tile with 128-byte swizzling (16-byte chunk c of key
+// row k stored at chunk c ^ (k & 7)).
+__device__ __forceinline__ const unsigned char* sw_addr(const unsigned char* tile, int row, int chunk) {
+  return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <int HD>
+__device__ __forceinline__ void qk_scores_sw(float (&sc)[kKB / 8][4], const uint32_t (&qf)[HD / 16][4],
+                                             const unsigned char* K, int lane) {
+#pragma unroll
+  for (int nt = 0; nt < kKB / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  const int j = lane >> 3;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const unsigned char* tile = K + (kk >> 2) * (kKB * 128);
+#pragma unroll
+    for (int n2 = 0; n2 < kKB / 16; ++n2) {
+      uint32_t kf[4];
+      ldsm_x4(kf, sw_addr(tile, n2 * 16 + (j >> 1) * 8 + (lane & 7), (kk & 3) * 2 + (j & 1)));
+      mma16816(sc[2 * n2], qf[kk], kf[0], kf[1]);
+      mma16816(sc[2 * n2 + 1], qf[kk], kf[2], kf[3]);
+    }
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void pv_accum_sw(float (&o)[HD / 8][4], const float (&p)[kKB / 8][4],
+                                            const unsigned char* V, int lane) {
+  const int j = lane >> 3;
+#pragma unroll
+  for (int kt = 0; kt < kKB / 16; ++kt) {
+    uint32_t pa[4] = {pack_bf16(p[2 * kt][0], p[2 * kt][1]), pack_bf16(p[2 * kt][2], p[2 * kt][3]),
+                      pack_bf16(p[2 * kt + 1][0], p[2 * kt + 1][1]), pack_bf16(p[2 * kt + 1][2], p[2 * kt + 1][3])};
+#pragma unroll
+    for (int d2 = 0; d2 < HD / 16; ++d2) {
+      uint32_t vf[4];
+      ldsm_x4_t(vf, sw_addr(V + (d2 >> 2) * (kKB * 128), kt * 16 + (j & 1) * 8 + (lane & 7), (d2 & 3) * 2 + (j >> 1)));
+      mma16816(o[2 * d2], pa, vf[0], vf[1]);
+      mma16816(o[2 * d2 + 1], pa, vf[2], vf[3]);
+    }
+  }
+}
+
 template <int HD>
 __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HD / 16][4], const bf16* Q, int warp, int lane) {
   constexpr int LD = HD + 8;
@@ -183,22 +228,35 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HD / 16][4], const b
 
 // Prefix partials: CTA = (64 query vectors of one request and KV head, one
 // split of the prefix).  Query vector v of the request is recompute slot
-// off_r + v / G, query head kvh * G + v % G.  The split CTAs of a query tile
-// form one cluster (along z): after their streaming loops every CTA sends its
-// partial state (max, denominator, unnormalised output) of each query row to
-// the CTA that owns the row, and each owner merges the S states in rank order
-// and writes one merged state per query to split slot 0.
+// off_r + v / G, query head kvh * G + v % G.  K/V blocks of 64 keys stream
+// through a kStages-deep ring of TMA loads (one (64-dim, 1-head, 64-key) box
+// per 64-dim half); the split CTAs of a query tile form one cluster (along z):
+// after their streaming loops every CTA sends its partial state (max,
+// denominator, unnormalised output) of each query row to the CTA that owns
+// the row, and each owner merges the S states in rank order and writes one
+// merged state per query.
+constexpr int kStages = 2;
+
 template <int HD>
-__global__ void __launch_bounds__(128) attn_prefix_mma(const AttnArgs a) {
-  pdl_wait();
-  pdl_trigger();
+constexpr int prefix_smem_bytes() {
+  return kStages * 2 * (HD / 64) * (kKB * 128) + kQT * (HD + 8) * 2 + 64 + 1024;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ CUtensorMap tmK,
+                                                       const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
   constexpr int LD = HD + 8;
   constexpr int XLD = HD + 2;  // exchange row: o[HD], m, l
-  extern __shared__ __align__(16) unsigned char smem[];
-  bf16* sQ = reinterpret_cast<bf16*>(smem);
-  bf16* sK = sQ + kQT * LD;
-  bf16* sV = sK + 2 * kKB * LD;
-  float* xbuf = reinterpret_cast<float*>(sK);  // exchange area, reused after the loop
+  constexpr int KTILE = kKB * 128;
+  constexpr int STAGE = 2 * (HD / 64) * KTILE;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  bf16* sQ = reinterpret_cast<bf16*>(base + kStages * STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + kStages * STAGE + kQT * LD * 2);
+  float* xbuf = reinterpret_cast<float*>(base);  // exchange area, reused after the loop
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
   const Splits sp = fixed_splits(a.P);
@@ -207,103 +265,98 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const AttnArgs a) {
   const int q0 = blockIdx.x * kQT;
   if (q0 >= nqv) return;  // uniform over the cluster
   const int s = sp.S > 1 ? (int)cluster_rank() : 0;
-  const bool has_keys = s < sp.S;
-  const int k_lo = s * sp.len, k_hi = has_keys ? min(a.P, k_lo + sp.len) : k_lo;
+  const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
+  const int nblk = k_hi > k_lo ? (k_hi - k_lo + kKB - 1) / kKB : 0;
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
-  const bf16* pk = reinterpret_cast<const bf16*>(a.pk) + ((size_t)r * a.P * a.nkv + kvh) * HD;
-  const bf16* pv = reinterpret_cast<const bf16*>(a.pv) + ((size_t)r * a.P * a.nkv + kvh) * HD;
-  const size_t kstride = (size_t)a.nkv * HD;
+
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) tc::mbar_init(&full[st], 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int b) {  // thread 0: K and V of key block b into its stage
+    const int st = b % kStages;
+    unsigned char* sk = base + st * STAGE;
+    const int z = r * a.P + k_lo + b * kKB;
+    tc::mbar_expect_tx(&full[st], STAGE);
+#pragma unroll
+    for (int h = 0; h < HD / 64; ++h) {
+      tc::tma_load_3d(sk + h * KTILE, &tmK, h * 64, kvh, z, &full[st]);
+      tc::tma_load_3d(sk + (HD / 64 + h) * KTILE, &tmV, h * 64, kvh, z, &full[st]);
+    }
+  };
+  if (tid == 0)
+    for (int b = 0; b < min(kStages - 1, nblk); ++b) issue(b);
+
+  for (int idx = tid; idx < kQT * (HD / 8); idx += 128) {
+    const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (v < nqv) {
+      const int g = off_r + v / G, h = kvh * G + v % G;
+      val = *reinterpret_cast<const uint4*>(qkv + (size_t)g * a.ld_qkv + h * HD + c8 * 8);
+    }
+    *reinterpret_cast<uint4*>(sQ + row * LD + c8 * 8) = val;
+  }
+  __syncthreads();
+  uint32_t qf[HD / 16][4];
+  load_q_frags<HD>(qf, sQ, warp, lane);
 
   float o[HD / 8][4];
 #pragma unroll
   for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  if (has_keys) {
-    for (int idx = tid; idx < kQT * (HD / 8); idx += 128) {
-      const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (v < nqv) {
-        const int g = off_r + v / G, h = kvh * G + v % G;
-        val = *reinterpret_cast<const uint4*>(qkv + (size_t)g * a.ld_qkv + h * HD + c8 * 8);
+  for (int b = 0; b < nblk; ++b) {
+    if (tid == 0 && b + kStages - 1 < nblk) issue(b + kStages - 1);  // its stage was freed by the last barrier
+    // a wait that gives up raises the error word but does not leave the loop,
+    // so every warp keeps reaching the same barriers
+    tc::mbar_wait(&full[b % kStages], (b / kStages) & 1, a.err);
+    const unsigned char* sk = base + (b % kStages) * STAGE;
+    float sc[kKB / 8][4];
+    qk_scores_sw<HD>(sc, qf, sk, lane);
+    const int kb0 = k_lo + b * kKB;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < kKB / 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = kb0 + nt * 8 + (lane & 3) * 2 + (e & 1);
+        sc[nt][e] = key < k_hi ? sc[nt][e] * a.scale_log2 : -INFINITY;
       }
-      *reinterpret_cast<uint4*>(sQ + row * LD + c8 * 8) = val;
+      mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
     }
-    auto load_kv = [&](int buf, int kb0) {
-      for (int idx = tid; idx < kKB * (HD / 8); idx += 128) {
-        const int jk = idx / (HD / 8), c8 = idx % (HD / 8), key = kb0 + jk;
-        bf16* dk = sK + (buf * kKB + jk) * LD + c8 * 8;
-        bf16* dv = sV + (buf * kKB + jk) * LD + c8 * 8;
-        if (key < k_hi) {
-          cp_async16(dk, pk + key * kstride + c8 * 8);
-          cp_async16(dv, pv + key * kstride + c8 * 8);
-        } else {
-          *reinterpret_cast<uint4*>(dk) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(dv) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      cp_async_commit();
-    };
-    const int nblk = k_hi > k_lo ? (k_hi - k_lo + kKB - 1) / kKB : 0;
-    if (nblk > 0) load_kv(0, k_lo);
+    const float n0 = fmaxf(m0, quad_max(mx0)), n1 = fmaxf(m1, quad_max(mx1));
+    const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < kKB / 8; ++nt) {
+      sc[nt][0] = exp2f(sc[nt][0] - n0);
+      sc[nt][1] = exp2f(sc[nt][1] - n0);
+      sc[nt][2] = exp2f(sc[nt][2] - n1);
+      sc[nt][3] = exp2f(sc[nt][3] - n1);
+      s0 += sc[nt][0] + sc[nt][1];
+      s1 += sc[nt][2] + sc[nt][3];
+    }
+    l0 = l0 * c0 + s0;
+    l1 = l1 * c1 + s1;
+    m0 = n0;
+    m1 = n1;
+#pragma unroll
+    for (int nt = 0; nt < HD / 8; ++nt) {
+      o[nt][0] *= c0;
+      o[nt][1] *= c0;
+      o[nt][2] *= c1;
+      o[nt][3] *= c1;
+    }
+    pv_accum_sw<HD>(o, sc, sk + (HD / 64) * KTILE, lane);
     __syncthreads();
-    uint32_t qf[HD / 16][4];
-    load_q_frags<HD>(qf, sQ, warp, lane);
-    for (int b = 0; b < nblk; ++b) {
-      if (b + 1 < nblk) {
-        load_kv((b + 1) & 1, k_lo + (b + 1) * kKB);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
-      __syncthreads();
-      float sc[kKB / 8][4];
-      qk_scores<HD>(sc, qf, sK + (b & 1) * kKB * LD, lane);
-      const int kb0 = k_lo + b * kKB;
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < kKB / 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = kb0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-          sc[nt][e] = key < k_hi ? sc[nt][e] * a.scale_log2 : -INFINITY;
-        }
-        mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-        mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-      }
-      const float n0 = fmaxf(m0, quad_max(mx0)), n1 = fmaxf(m1, quad_max(mx1));
-      const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < kKB / 8; ++nt) {
-        sc[nt][0] = exp2f(sc[nt][0] - n0);
-        sc[nt][1] = exp2f(sc[nt][1] - n0);
-        sc[nt][2] = exp2f(sc[nt][2] - n1);
-        sc[nt][3] = exp2f(sc[nt][3] - n1);
-        s0 += sc[nt][0] + sc[nt][1];
-        s1 += sc[nt][2] + sc[nt][3];
-      }
-      l0 = l0 * c0 + s0;
-      l1 = l1 * c1 + s1;
-      m0 = n0;
-      m1 = n1;
-#pragma unroll
-      for (int nt = 0; nt < HD / 8; ++nt) {
-        o[nt][0] *= c0;
-        o[nt][1] *= c0;
-        o[nt][2] *= c1;
-        o[nt][3] *= c1;
-      }
-      pv_accum<HD>(o, sc, sV + (b & 1) * kKB * LD, lane);
-      __syncthreads();
-    }
-    l0 = quad_sum(l0);
-    l1 = quad_sum(l1);
   }
+  l0 = quad_sum(l0);
+  l1 = quad_sum(l1);
 
-  if (sp.S == 1) {  // a single split: rank 0's partial is already the merged state
+  if (sp.S == 1) {  // a single split: the partial is already the merged state
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      if (!has_keys) break;
       const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
       if (v >= nqv) continue;
       const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
@@ -316,48 +369,43 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const AttnArgs a) {
         a.part_ml[qi * 2 + 1] = half ? l1 : l0;
       }
     }
-    return;  // uniform over the cluster: S is computed from the same counts
+    return;
   }
   // rows [rank * per, (rank + 1) * per) of the tile are merged by `rank`
   const int per = (kQT + sp.S - 1) / sp.S;
   cluster_sync_all();  // every CTA is past its loop: exchange areas are free
-  if (has_keys) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int vr = warp * 16 + (lane >> 2) + half * 8;  // row within the tile
-      const int owner = vr / per;
-      const uint32_t base =
-          map_rank(smem_addr(xbuf + ((size_t)s * per + (vr - owner * per)) * XLD), (uint32_t)owner);
+  for (int half = 0; half < 2; ++half) {
+    const int vr = warp * 16 + (lane >> 2) + half * 8;  // row within the tile
+    const int owner = vr / per;
+    const uint32_t dst = map_rank(smem_addr(xbuf + ((size_t)s * per + (vr - owner * per)) * XLD), (uint32_t)owner);
 #pragma unroll
-      for (int nt = 0; nt < HD / 8; ++nt)
-        st_cluster_v2(base + (nt * 8 + (lane & 3) * 2) * 4, o[nt][2 * half], o[nt][2 * half + 1]);
-      if ((lane & 3) == 0) {
-        st_cluster_f32(base + HD * 4, half ? m1 : m0);
-        st_cluster_f32(base + (HD + 1) * 4, half ? l1 : l0);
-      }
+    for (int nt = 0; nt < HD / 8; ++nt)
+      st_cluster_v2(dst + (nt * 8 + (lane & 3) * 2) * 4, o[nt][2 * half], o[nt][2 * half + 1]);
+    if ((lane & 3) == 0) {
+      st_cluster_f32(dst + HD * 4, half ? m1 : m0);
+      st_cluster_f32(dst + (HD + 1) * 4, half ? l1 : l0);
     }
   }
   cluster_sync_all();  // every partial has arrived
-  if (has_keys) {
-    const int rows = min(per, kQT - s * per);
-    for (int idx = tid; idx < rows * HD; idx += 128) {
-      const int rl = idx / HD, dd = idx % HD, v = q0 + s * per + rl;
-      if (v >= nqv) continue;
-      float M = -INFINITY;
-      for (int t = 0; t < sp.S; ++t) M = fmaxf(M, xbuf[((size_t)t * per + rl) * XLD + HD]);
-      float acc = 0.f, l = 0.f;
-      for (int t = 0; t < sp.S; ++t) {
-        const float* x = xbuf + ((size_t)t * per + rl) * XLD;
-        const float w = exp2f(x[HD] - M);  // 0 for an empty split
-        acc += w * x[dd];
-        l += w * x[HD + 1];
-      }
-      const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
-      a.part_o[qi * HD + dd] = acc;
-      if (dd == 0) {
-        a.part_ml[qi * 2 + 0] = M;
-        a.part_ml[qi * 2 + 1] = l;
-      }
+  const int rows = min(per, kQT - s * per);
+  for (int idx = tid; idx < rows * HD; idx += 128) {
+    const int rl = idx / HD, dd = idx % HD, v = q0 + s * per + rl;
+    if (v >= nqv) continue;
+    float M = -INFINITY;
+    for (int t = 0; t < sp.S; ++t) M = fmaxf(M, xbuf[((size_t)t * per + rl) * XLD + HD]);
+    float acc = 0.f, l = 0.f;
+    for (int t = 0; t < sp.S; ++t) {
+      const float* x = xbuf + ((size_t)t * per + rl) * XLD;
+      const float w = exp2f(x[HD] - M);
+      acc += w * x[dd];
+      l += w * x[HD + 1];
+    }
+    const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+    a.part_o[qi * HD + dd] = acc;
+    if (dd == 0) {
+      a.part_ml[qi * 2 + 0] = M;
+      a.part_ml[qi * 2 + 1] = l;
     }
   }
 }
@@ -616,11 +664,10 @@ template <int HD>
 cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   constexpr int LD = HD + 8;
   const int G = a.nq / a.nkv;
-  const size_t smem_p = (size_t)(kQT + 4 * kKB) * LD * sizeof(bf16);
   const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16);
   static cudaError_t attr = [&] {
     cudaError_t e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)((kQT + 4 * kKB) * LD * sizeof(bf16)));
+                                         prefix_smem_bytes<HD>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
@@ -628,11 +675,16 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   }();
   if (attr != cudaSuccess) return lc.err = attr;
   if (a.P > 0) {
+    alignas(64) CUtensorMap tmK, tmV;
+    if (!make_tmap_kv(&tmK, a.pk, HD, a.nkv, (uint64_t)a.R * a.P) ||
+        !make_tmap_kv(&tmV, a.pv, HD, a.nkv, (uint64_t)a.R * a.P))
+      return lc.err = cudaErrorInvalidValue;
     // worst case: every row of a request recomputes
     const Splits sp = fixed_splits(a.P);
     dim3 grid((a.Bp * a.L * G + kQT - 1) / kQT, a.R * a.nkv, sp.S);
     lc.before(SF_K_ATTN_PREFIX);
-    lc.check(launch_pdl(lc.st, grid, dim3(128), smem_p, sp.S, attn_prefix_mma<HD>, a));
+    lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD>(), sp.S, attn_prefix_mma<HD>, tmK,
+                        tmV, a));
     lc.after(SF_K_ATTN_PREFIX);
   }
   dim3 grid((a.L * G + kBQT - 1) / kBQT, a.R * a.Bp * a.nkv);

@@ -323,6 +323,20 @@ int max_active_clusters(int s) {
 // K splits for an M x K weight over n_tiles row tiles: the largest cluster
 // size that keeps every (m, n) tile resident in one wave and gives each CTA
 // at least one K block.
+// Prefix keys or values of one layer, [rows = R * P][nkv][hd] bf16, as a 3-D
+// TMA source with (64 dims, 1 head, 64 keys) boxes and 128-byte swizzling.
+bool make_tmap_kv(CUtensorMap* tm, const void* base, int hd, int nkv, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn || hd % 64 != 0 || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)nkv, rows};
+  cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)nkv * hd * 2};
+  cuuint32_t box[3] = {64u, 1u, 64u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int gemm_tc_splits(int M, int K, int n_tiles) {
   const int m_tiles = M / tc::BM, nk = K / tc::BK, tiles = std::max(1, m_tiles * n_tiles);
   const int want = std::min(sm_count() / tiles, nk);

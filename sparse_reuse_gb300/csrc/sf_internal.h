@@ -184,6 +184,7 @@ struct TcGemm {
 };
 bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 int gemm_tc_splits(int M, int K, int n_tiles);
+bool make_tmap_kv(CUtensorMap* tm, const void* base, int hd, int nkv, uint64_t rows);
 cudaError_t launch_gemm_tc(Launch& lc, int fam, const TcGemm& g, EpiKind kind, const EpiArgs& e);
 
 // sf_gemm.cu (FP32 contexts)
