@@ -118,8 +118,9 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.6)   # nvidia-smi is sampling before the timed region starts
         except Exception:
             self.proc = None
         return self
@@ -127,7 +128,6 @@ class ClockSampler:
     def __exit__(self, *exc):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -247,7 +247,7 @@ def sweep(args, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="1.5b")

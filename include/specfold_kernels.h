@@ -27,7 +27,7 @@ extern "C" {
  *   count      device int32 holding the live row count (<= rows_cap), or NULL
  *              to use dense_count.
  *   Y          device fp32 [rows_cap][ldy], ldy >= M; rows >= count untouched.
- *   splits     1..6 or 8, at most K/64: K is split over a cluster of this
+ *   splits     1..8, at most K/64: K is split over a cluster of this
  *              many CTAs per output tile, whose partial sums are added in
  *              cluster-rank order in shared memory (no workspace).
  *   err        device uint32 error word (bit 32 = a bounded wait gave up) or NULL.

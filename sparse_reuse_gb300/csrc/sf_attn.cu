@@ -14,9 +14,9 @@
 //      its block part runs over the branch's own L block keys/values, read
 //      through the source slots of the branch's positions, and is merged with
 //      the query's prefix partials by log-sum-exp.
-// The split count S is derived on the device from the live recompute count,
-// identically in both kernels, so small recompute sets still fill the GPU and
-// large ones do not pay for partials they do not need.
+// The tensor-core path fixes the split count S from the prefix length (a
+// cluster of S CTAs per query tile); the CUDA-core path derives S on the
+// device from the live recompute count, identically in both of its kernels.
 //
 // BF16 contexts run both kernels on the tensor cores (mma.sync m16n8k16, bf16
 // in, fp32 accumulate); the GQA group's query heads are packed into the M

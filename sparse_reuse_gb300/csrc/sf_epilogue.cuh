@@ -132,26 +132,32 @@ struct EpiStore {
   }
 };
 
-// Epilogue of the 32-row chunk starting at row0 for the rows jj = ew + 4b
-// (b = 0..7, jj < nvalid) handled by epilogue warp ew: the global reads of all
-// eight rows are issued before any is consumed.  getv(jj, v) supplies the
-// fp32 accumulators of row jj for this lane's four features.
-template <class Epi, class GetV>
-__device__ __forceinline__ void epilogue_chunk(const typename Epi::Params& ep, int row0, int nvalid, int m0,
-                                               int ew, int lane, GetV getv) {
-  typename Epi::Pre pre[8];
+// Epilogue of up to 32 rows row0 + stride * jj, jj < nvalid; epilogue warp ew
+// handles jj = ew + 4b (b = 0..7).  epilogue_prefetch() issues the global reads
+// of all of them (it can run before the accumulators are ready, e.g. while the
+// main loop streams the weights); epilogue_apply() consumes them, with getv(jj,
+// v) supplying the fp32 accumulators of row jj for this lane's four features.
+template <class Epi>
+__device__ __forceinline__ void epilogue_prefetch(const typename Epi::Params& ep, int row0, int stride, int nvalid,
+                                                  int m0, int ew, int lane, typename Epi::Pre (&pre)[8]) {
 #pragma unroll
   for (int b = 0; b < 8; ++b) {
     const int jj = ew + 4 * b;
-    if (jj < nvalid) Epi::prefetch(ep, row0 + jj, m0, lane, pre[b]);
+    if (jj < nvalid) Epi::prefetch(ep, row0 + jj * stride, m0, lane, pre[b]);
   }
+}
+
+template <class Epi, class GetV>
+__device__ __forceinline__ void epilogue_apply(const typename Epi::Params& ep, int row0, int stride, int nvalid,
+                                               int m0, int ew, int lane, const typename Epi::Pre (&pre)[8],
+                                               GetV getv) {
 #pragma unroll
   for (int b = 0; b < 8; ++b) {
     const int jj = ew + 4 * b;
     if (jj < nvalid) {
       float vv[4];
       getv(jj, vv);
-      Epi::apply(ep, row0 + jj, m0, lane, vv, pre[b]);
+      Epi::apply(ep, row0 + jj * stride, m0, lane, vv, pre[b]);
     }
   }
 }

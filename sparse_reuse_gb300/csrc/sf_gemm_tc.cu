@@ -4,12 +4,15 @@
 // The weight is the M operand: each CTA owns 128 output features (TMEM lanes)
 // and up to 256 rows (TMEM columns), so a weight tile is streamed once for all
 // rows of a layer; the rows are the N operand, loaded in 64-row TMA boxes only
-// up to the live row count.  Narrow GEMMs split K over the CTAs of a thread
-// block cluster (along grid z); after the main loops every CTA pushes its
-// partial accumulators, 32 rows at a time, into the shared memory of the CTA
-// that owns those rows (distributed shared memory), and each owner adds the
-// partials in cluster-rank order before the epilogue, so the result does not
-// depend on scheduling and no global workspace is used.
+// up to the live row count, and as many pipeline stages as the shared memory
+// holds for that count.  Narrow GEMMs split K over the CTAs of a thread block
+// cluster (along grid z); after the main loops every CTA pushes the partial
+// accumulator of row j into the shared memory of cluster rank j % S, which
+// finishes that row (distributed shared memory): each owner adds the partials
+// in cluster-rank order before the epilogue, so the result does not depend on
+// scheduling, no global workspace is used and the epilogue work is spread over
+// every rank of the cluster.  The epilogue's own global reads (rotary table,
+// residual rows) are issued while the main loop runs.
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the
 // MMAs, warps 2-5 drain TMEM into the layer epilogue.
@@ -30,20 +33,34 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN = 256;
 constexpr int RC = 64;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_CHUNK = RC * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
 constexpr int THREADS = 192;
-constexpr int PIPE_BYTES = STAGES * (A_BYTES + B_BYTES);
+// The pipeline's shared memory holds a ring of weight (A) tiles growing up from
+// its start and a ring of row (B) tiles growing down from its end; the number
+// of stages follows from the live row count, so a small recompute set keeps
+// up to MAX_STAGES weight tiles in flight and a full 256-row tile still has
+// MIN_STAGES.  Weight tiles fetched before the row count is known go to the
+// first MIN_STAGES slots of the A ring, which every stage count keeps.
+constexpr int MAX_STAGES = 12;
+constexpr int MIN_STAGES = 4;
+constexpr int PIPE_BYTES = 216 * 1024;
 constexpr int SMEM_BYTES = PIPE_BYTES + 1024 + 256;
+static_assert(MIN_STAGES * (A_BYTES + (BN / RC) * B_CHUNK) <= PIPE_BYTES, "a full row tile needs MIN_STAGES");
+static_assert(2 * MAX_STAGES * 8 + 8 + 4 <= 256, "barrier area");
+
+__host__ __device__ constexpr int stages_for(int n_chunks) {
+  return n_chunks <= 0 ? MIN_STAGES
+                       : (PIPE_BYTES / (A_BYTES + n_chunks * B_CHUNK) < MAX_STAGES
+                              ? PIPE_BYTES / (A_BYTES + n_chunks * B_CHUNK)
+                              : MAX_STAGES);
+}
 constexpr int STAGE_LD = 129;            // epilogue staging row stride (floats)
-constexpr int CHUNK_BYTES = 32 * BM * 4;  // 32 rows x 128 features of fp32 partials
 
 // Split counts whose exchange buffers fit the pipeline's shared memory for a
-// full 256-row tile: S * ceil(8 / S) chunks of 32 rows.
+// full 256-row tile: S * ceil(256 / S) rows of 128 fp32 partials.
 __host__ __device__ constexpr bool split_fits(int S) {
-  return S >= 1 && S <= 8 && S * ((8 + S - 1) / S) * CHUNK_BYTES <= PIPE_BYTES;
+  return S >= 1 && S <= 8 && S * ((BN + S - 1) / S) * BM * 4 <= PIPE_BYTES;
 }
 
 struct Params {
@@ -61,11 +78,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + PIPE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* tfull = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,7 +104,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -103,11 +118,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   // weight tiles of the first stages do not depend on earlier kernels: start
   // streaming them before waiting for the kernel that produced the rows
-  const int npre = lead ? min(STAGES, kb1 - kb0) : 0;
+  const int npre = lead ? min(MIN_STAGES, kb1 - kb0) : 0;
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < npre; ++it) {
       mbar_expect_tx_only(&full[it], A_BYTES);
-      tma_load_2d(sA + it * A_BYTES, &tmA, (kb0 + it) * BK, m0, &full[it]);
+      tma_load_2d(smem + it * A_BYTES, &tmA, (kb0 + it) * BK, m0, &full[it]);
     }
   }
   if (lead) {
@@ -119,11 +134,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_rows = active ? min(BN, count - row0) : 0;
   const int n_mma = (n_rows + 15) & ~15;
   const int n_chunks = (n_rows + RC - 1) / RC;
+  const int nst = stages_for(n_chunks);  // uniform over the cluster
+  auto sA = [&](int st) { return smem + st * A_BYTES; };
+  auto sB = [&](int st) { return smem + PIPE_BYTES - (st + 1) * n_chunks * B_CHUNK; };
   const int q = warp & 3;
   const int f = q * 32 + lane;
   const int ew = warp - 2;
   const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
   bool go = true;
+  // rows own0 + S * t (t < n_own) of the tile are finished by this CTA: all of
+  // them without a split, every S-th one (cluster rank z first) with one
+  const int own0 = S > 1 ? z : 0;
+  const int n_own = n_rows > own0 ? (n_rows - own0 + S - 1) / S : 0;
+  typename Epi::Pre pre[8];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -135,39 +158,46 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait(&full[it], 0, p.err);
         }
       } else {
+        int s = 0;
+        uint32_t ph = 0;  // stage it % nst and parity of it / nst, advanced without division
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
           if (it < npre) {
             mbar_expect_tx(&full[s], n_chunks * B_CHUNK);
           } else {
             if (!mbar_wait(&empty[s], ph ^ 1, p.err)) break;
             mbar_expect_tx(&full[s], A_BYTES + n_chunks * B_CHUNK);
-            tma_load_2d(sA + s * A_BYTES, &tmA, kb * BK, m0, &full[s]);
+            tma_load_2d(sA(s), &tmA, kb * BK, m0, &full[s]);
           }
           for (int c = 0; c < n_chunks; ++c)
-            tma_load_2d(sB + s * B_BYTES + c * B_CHUNK, &tmB, kb * BK, row0 + c * RC, &full[s]);
+            tma_load_2d(sB(s) + c * B_CHUNK, &tmB, kb * BK, row0 + c * RC, &full[s]);
+          if (++s == nst) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         // every copy this CTA issued lands before its shared memory is reused
-        for (int j = max(0, it - STAGES); j < it; ++j) mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.err);
+        for (int j = max(0, it - nst); j < it; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, p.err);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && active) {
       const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
-      int it = 0;
+      int it = 0, s = 0;
+      uint32_t ph = 0;
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
         if (!mbar_wait(&full[s], ph, p.err)) break;
         fence_after_sync();
-        const uint64_t da = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
-        const uint64_t db = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES));
+        const uint64_t da = sw128_kmajor_desc(smem_u32(sA(s)));
+        const uint64_t db = sw128_kmajor_desc(smem_u32(sB(s)));
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
           mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
+        if (++s == nst) {
+          s = 0;
+          ph ^= 1;
+        }
       }
       mma_commit(tfull);
       // TMEM and shared memory are reused only after every MMA has completed
@@ -175,6 +205,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else if (active) {
+    // the epilogue's global reads for this warp's first rows are issued while
+    // the main loop streams the weights
+    epilogue_prefetch<Epi>(ep, row0 + own0, S, min(32, n_own), m0, ew, lane, pre);
     go = mbar_wait(tfull, 0, p.err);
     fence_after_sync();
     if (S == 1 && go) {
@@ -185,46 +218,57 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) stage[j * STAGE_LD + f] = v[j];
         named_bar_sync(1, 128);
-        epilogue_chunk<Epi>(ep, row0 + j0, min(32, n_rows - j0), m0, ew, lane, [&](int jj, float (&vv)[4]) {
+        if (j0 > 0) epilogue_prefetch<Epi>(ep, row0 + j0, 1, min(32, n_rows - j0), m0, ew, lane, pre);
+        epilogue_apply<Epi>(ep, row0 + j0, 1, min(32, n_rows - j0), m0, ew, lane, pre,
+                            [&](int jj, float (&vv)[4]) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) vv[c] = stage[jj * STAGE_LD + lane + 32 * c];
-        });
+                              for (int c = 0; c < 4; ++c) vv[c] = stage[jj * STAGE_LD + lane + 32 * c];
+                            });
         named_bar_sync(1, 128);
       }
     }
   }
 
   if (S > 1 && active) {
-    // chunk c (32 rows) belongs to cluster rank c % S, which keeps the
-    // partials of every rank for it at buf[rank][c / S][row][feature]
-    const int nc = (n_rows + 31) / 32;
-    const int n_own = (nc + S - 1) / S;
+    // row j of the tile is finished by cluster rank j % S, which keeps the
+    // partials of every rank for it at buf[rank][j / S][feature]
+    const int n_slot = (n_rows + S - 1) / S;
     float* buf = reinterpret_cast<float*>(smem);
-    if (threadIdx.x == 0 && (size_t)S * n_own * CHUNK_BYTES > (size_t)PIPE_BYTES) raise_error(p.err, kErrGemm);
+    const bool fits = (size_t)S * n_slot * BM * 4 <= (size_t)PIPE_BYTES;  // S * ceil(256 / S) rows always fit
+    if (threadIdx.x == 0 && !fits) raise_error(p.err, kErrGemm);
     fence_before_sync();
     cluster_sync_all();  // every CTA of the tile is past its main loop
-    if (warp >= 2 && go && (size_t)S * n_own * CHUNK_BYTES <= (size_t)PIPE_BYTES) {
-      for (int c = 0; c < nc; ++c) {
+    if (warp >= 2 && go && fits) {
+      const uint32_t mine = smem_u32(buf + (size_t)z * n_slot * BM + f);
+      int owner = 0, slot = 0;  // of row c * 32 + j, advanced row by row
+      for (int c = 0; c * 32 < n_rows; ++c) {
         float v[32];
         tmem_ld32(tbase + c * 32, v);
-        const uint32_t local = smem_u32(buf + ((size_t)(z * n_own + c / S) * 32) * BM + f);
-        const uint32_t remote = map_to_rank(local, (uint32_t)(c % S));
 #pragma unroll
-        for (int j = 0; j < 32; ++j) st_cluster_f32(remote + j * BM * 4, v[j]);
+        for (int j = 0; j < 32; ++j) {
+          if (c * 32 + j < n_rows)
+            st_cluster_f32(map_to_rank(mine + slot * BM * 4, (uint32_t)owner), v[j]);
+          if (++owner == S) {
+            owner = 0;
+            ++slot;
+          }
+        }
       }
     }
     cluster_sync_all();  // every partial has been delivered
-    if (warp >= 2 && (size_t)S * n_own * CHUNK_BYTES <= (size_t)PIPE_BYTES) {
-      for (int lc = 0; lc < n_own; ++lc) {
-        const int c = z + lc * S;
-        if (c >= nc) break;
-        epilogue_chunk<Epi>(ep, row0 + c * 32, min(32, n_rows - c * 32), m0, ew, lane,
+    if (warp >= 2 && go && fits) {
+      for (int t0 = 0; t0 < n_own; t0 += 32) {
+        if (t0 > 0) epilogue_prefetch<Epi>(ep, row0 + own0 + S * t0, S, min(32, n_own - t0), m0, ew, lane, pre);
+        epilogue_apply<Epi>(ep, row0 + own0 + S * t0, S, min(32, n_own - t0), m0, ew, lane, pre,
                             [&](int jj, float (&vv)[4]) {
                               vv[0] = vv[1] = vv[2] = vv[3] = 0.f;
-                              for (int s = 0; s < S; ++s) {
-                                const float* src = buf + ((size_t)(s * n_own + lc) * 32 + jj) * BM + lane;
+                              const float* src = buf + (size_t)(t0 + jj) * BM + lane;
 #pragma unroll
-                                for (int cc = 0; cc < 4; ++cc) vv[cc] += src[32 * cc];
+                              for (int r = 0; r < 8; ++r) {
+                                if (r < S) {
+#pragma unroll
+                                  for (int cc = 0; cc < 4; ++cc) vv[cc] += src[(size_t)r * n_slot * BM + 32 * cc];
+                                }
                               }
                             });
       }

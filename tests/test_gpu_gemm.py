@@ -41,7 +41,7 @@ def test_counts_single_split(sf, count):
     _run(sf, 256, 512, 512, count, 1)
 
 
-@pytest.mark.parametrize("splits", [2, 3, 4, 5, 6, 8])
+@pytest.mark.parametrize("splits", [2, 3, 4, 5, 6, 7, 8])
 def test_split_k(sf, splits):
     _run(sf, 384, 1536, 300, 288, splits)
     _run(sf, 384, 1536, 300, 50, splits, seed=1)
@@ -65,9 +65,19 @@ def test_split_results_are_deterministic(sf):
 
 
 def test_bad_arguments_rejected(sf):
+    # every buffer is real and larger than any launch these arguments describe
+    X = torch.zeros((256, 1024), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((256, 1024), dtype=torch.bfloat16, device="cuda")
+    Y = torch.zeros((256, 256), device="cuda")
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    x, w, y, e = X.data_ptr(), W.data_ptr(), Y.data_ptr(), err.data_ptr()
     with pytest.raises(sf.SpecFoldError):
-        sf.sfk_gemm_bf16(None, 16, 64, 16, 100, 64, None, 1, 16, 100, 1)      # M not a multiple of 128
+        sf.sfk_gemm_bf16(None, x, 64, w, 100, 64, None, 1, y, 100, 1, e)       # M not a multiple of 128
     with pytest.raises(sf.SpecFoldError):
-        sf.sfk_gemm_bf16(None, 16, 64, 16, 128, 64, None, 1, 16, 128, 2)      # more splits than K blocks
+        sf.sfk_gemm_bf16(None, x, 64, w, 128, 64, None, 1, y, 128, 2, e)       # more splits than K blocks
     with pytest.raises(sf.SpecFoldError):
-        sf.sfk_gemm_bf16(None, 16, 64, 16, 128, 1024, None, 1, 16, 128, 7)    # cluster size without room
+        sf.sfk_gemm_bf16(None, x, 64, w, 128, 1024, None, 1, y, 128, 9, e)     # cluster larger than 8
+    with pytest.raises(sf.SpecFoldError):
+        sf.sfk_gemm_bf16(None, x, 64, w, 128, 1024, None, 1, y, 128, 0, e)     # no split at all
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
