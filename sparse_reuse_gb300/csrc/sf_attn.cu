@@ -68,6 +68,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 16-byte asynchronous copy global -> shared through L2 only (zero-filled
+// when !valid; src must still point into a live allocation).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -91,15 +103,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ float quad_max(float v) {
@@ -255,15 +258,20 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   bf16* sQ = reinterpret_cast<bf16*>(base + kStages * STAGE);
   uint64_t* full = reinterpret_cast<uint64_t*>(base + kStages * STAGE + kQT * LD * 2);
   float* xbuf = reinterpret_cast<float*>(base);  // exchange area, reused after the loop
-  pdl_wait();
-  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
   const Splits sp = fixed_splits(a.P);
   const int G = a.nq / a.nkv;
-  const int off_r = a.meta[1 + r], nqv = (a.meta[2 + r] - off_r) * G;
+  // Every kernel of the pass lets its dependants start only after its own
+  // dependency wait, so the kernels before the previous one have completed
+  // when this grid starts: the recompute offsets (gate kernel) can be read
+  // before the wait, past L1.  Only the queries (previous kernel) wait.
+  const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
   const int q0 = blockIdx.x * kQT;
-  if (q0 >= nqv) return;  // uniform over the cluster
+  if (q0 >= nqv) {  // uniform over the cluster
+    pdl_wait();
+    return;
+  }
   const int s = sp.S > 1 ? (int)cluster_rank() : 0;
   const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
   const int nblk = k_hi > k_lo ? (k_hi - k_lo + kKB - 1) / kKB : 0;
@@ -285,18 +293,20 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
       tc::tma_load_3d(sk + (HD / 64 + h) * KTILE, &tmV, h * 64, kvh, z, &full[st]);
     }
   };
+  // the prefix keys and values are inputs of the pass
   if (tid == 0)
     for (int b = 0; b < min(kStages - 1, nblk); ++b) issue(b);
+  pdl_wait();
+  pdl_trigger();
 
   for (int idx = tid; idx < kQT * (HD / 8); idx += 128) {
     const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (v < nqv) {
-      const int g = off_r + v / G, h = kvh * G + v % G;
-      val = *reinterpret_cast<const uint4*>(qkv + (size_t)g * a.ld_qkv + h * HD + c8 * 8);
-    }
-    *reinterpret_cast<uint4*>(sQ + row * LD + c8 * 8) = val;
+    const bool ok = v < nqv;
+    const int g = off_r + (ok ? v / G : 0), h = kvh * G + (ok ? v % G : 0);
+    cp_async16(sQ + row * LD + c8 * 8, qkv + (size_t)g * a.ld_qkv + h * HD + c8 * 8, ok);
   }
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   uint32_t qf[HD / 16][4];
   load_q_frags<HD>(qf, sQ, warp, lane);
@@ -418,24 +428,31 @@ constexpr int kBQT = 32;
 
 template <int HD>
 __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
-  pdl_wait();
-  pdl_trigger();
   constexpr int LD = HD + 8;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int slot[kKB];
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   bf16* sK = sQ + kBQT * LD;
   bf16* sV = sK + kKB * LD;
+  float* sP = reinterpret_cast<float*>(sV + kKB * LD);  // [kBQT][HD] merged prefix outputs
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rb = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;  // rb = r * Bp + i
   const int G = a.nq / a.nkv, L = a.L;
   const int q0 = blockIdx.x * kBQT, nqv = L * G;
-  if (q0 >= nqv) return;
-  const int count = a.meta[0];
+  if (q0 >= nqv) {
+    pdl_wait();
+    return;
+  }
+  // Every kernel of the pass lets its dependants start only after its own
+  // dependency wait, so the kernels before the previous one have completed
+  // when this grid starts: the source slots (gate kernel) are read before the
+  // wait, past L1, and so are the projected rows when the prefix kernel sits
+  // between the projection and this one.
+  const int count = __ldcg(a.meta);
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
   const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
   for (int m = tid; m < kKB; m += 64) {
-    int g = m < L ? a.rcslot[rb * L + m] : 0;
+    int g = m < L ? __ldcg(a.rcslot + rb * L + m) : 0;
     if (g < 0 || g >= count) {
       raise_error(a.err, kErrAttn);
       g = 0;
@@ -443,24 +460,47 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
     slot[m] = g;
   }
   __syncthreads();
-  for (int idx = tid; idx < kBQT * (HD / 8); idx += 64) {
-    const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (v < nqv)
-      val = *reinterpret_cast<const uint4*>(qkv + (size_t)slot[v / G] * a.ld_qkv + (kvh * G + v % G) * HD + c8 * 8);
-    *reinterpret_cast<uint4*>(sQ + row * LD + c8 * 8) = val;
-  }
-  for (int idx = tid; idx < kKB * (HD / 8); idx += 64) {
-    const int m = idx / (HD / 8), c8 = idx % (HD / 8);
-    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (m < L) {
-      const bf16* src = qkv + (size_t)slot[m] * a.ld_qkv;
-      kv = *reinterpret_cast<const uint4*>(src + koff + c8 * 8);
-      vv = *reinterpret_cast<const uint4*>(src + voff + c8 * 8);
+  auto load_rows = [&] {
+    for (int idx = tid; idx < kBQT * (HD / 8); idx += 64) {
+      const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
+      const bool ok = v < nqv;
+      cp_async16(sQ + row * LD + c8 * 8,
+                 qkv + (size_t)slot[ok ? v / G : 0] * a.ld_qkv + (kvh * G + (ok ? v % G : 0)) * HD + c8 * 8, ok);
     }
-    *reinterpret_cast<uint4*>(sK + m * LD + c8 * 8) = kv;
-    *reinterpret_cast<uint4*>(sV + m * LD + c8 * 8) = vv;
+    for (int idx = tid; idx < kKB * (HD / 8); idx += 64) {
+      const int m = idx / (HD / 8), c8 = idx % (HD / 8);
+      const bf16* src = qkv + (size_t)slot[m] * a.ld_qkv;
+      cp_async16(sK + m * LD + c8 * 8, src + koff + c8 * 8, m < L);
+      cp_async16(sV + m * LD + c8 * 8, src + voff + c8 * 8, m < L);
+    }
+    cp_async_commit();
+  };
+  if (a.P > 0) load_rows();
+  pdl_wait();
+  pdl_trigger();
+  if (a.P == 0) load_rows();
+  // the merged prefix state of each query (previous kernel), needed only
+  // after the block part: its output rows are copied while that runs
+  float mp[2] = {0.f, 0.f}, lp[2] = {0.f, 0.f};
+  if (a.P > 0) {
+    for (int idx = tid; idx < kBQT * (HD / 4); idx += 64) {
+      const int row = idx / (HD / 4), c4 = idx % (HD / 4), v = q0 + row;
+      const bool ok = v < nqv;
+      const size_t qi = (size_t)slot[ok ? v / G : 0] * a.nq + kvh * G + (ok ? v % G : 0);
+      cp_async16(sP + row * HD + c4 * 4, a.part_o + qi * HD + c4 * 4, ok);
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
+      if (v < nqv) {
+        const size_t qi = (size_t)slot[v / G] * a.nq + kvh * G + v % G;
+        mp[half] = a.part_ml[qi * 2];
+        lp[half] = a.part_ml[qi * 2 + 1];
+      }
+    }
   }
+  cp_async_commit();
+  cp_async_wait<1>();  // the projected rows have landed
   __syncthreads();
   uint32_t qf[HD / 16][4];
   load_q_frags<HD>(qf, sQ, warp, lane);
@@ -493,6 +533,8 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
 #pragma unroll
   for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   pv_accum<HD>(o, sc, sV, lane);
+  cp_async_wait<0>();  // the prefix outputs have landed
+  __syncthreads();
 
   bf16* out = reinterpret_cast<bf16*>(a.attn);
 #pragma unroll
@@ -500,22 +542,19 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
     const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
     if (v >= nqv) continue;
     const int row = rb * L + v / G, h = kvh * G + v % G;
-    const int g = slot[v / G];
     const float mb = half ? mb1 : mb0, lb = half ? lb1 : lb0;
     float acc[HD / 8][2];
     float l, wb;
     if (a.P > 0) {
-      // the merged prefix state of this query (one per recompute slot and head)
-      const size_t qi = (size_t)g * a.nq + h;
-      const float mp = a.part_ml[qi * 2], lp = a.part_ml[qi * 2 + 1];
+      // merge with the prefix state of this query (one per recompute slot and head)
       float2 pp[HD / 8];
-      const float* po = a.part_o + qi * HD + (lane & 3) * 2;
+      const float* po = sP + (v - q0) * HD + (lane & 3) * 2;
 #pragma unroll
       for (int nt = 0; nt < HD / 8; ++nt) pp[nt] = *reinterpret_cast<const float2*>(po + nt * 8);
-      const float M = fmaxf(mb, mp);
+      const float M = fmaxf(mb, mp[half]);
       wb = exp2f(mb - M);
-      const float wp = exp2f(mp - M);
-      l = lb * wb + lp * wp;
+      const float wp = exp2f(mp[half] - M);
+      l = lb * wb + lp[half] * wp;
 #pragma unroll
       for (int nt = 0; nt < HD / 8; ++nt) {
         acc[nt][0] = o[nt][2 * half] * wb + wp * pp[nt].x;
@@ -664,13 +703,13 @@ template <int HD>
 cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   constexpr int LD = HD + 8;
   const int G = a.nq / a.nkv;
-  const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16);
+  const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16) + (size_t)kBQT * HD * sizeof(float);
   static cudaError_t attr = [&] {
     cudaError_t e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          prefix_smem_bytes<HD>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
+                               (int)((kBQT + 2 * kKB) * LD * sizeof(bf16) + kBQT * HD * sizeof(float)));
     return e;
   }();
   if (attr != cudaSuccess) return lc.err = attr;
