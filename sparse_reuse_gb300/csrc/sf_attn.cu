@@ -39,9 +39,9 @@ struct Splits {
 };
 
 // Tensor-core path: the split count is fixed on the host from the prefix
-// length alone (at most 512 keys per CTA), so the split CTAs of a query tile
+// length alone (at most 128 keys per CTA), so the split CTAs of a query tile
 // form a cluster of exactly that size.
-constexpr int kKeysPerSplit = 512;
+constexpr int kKeysPerSplit = 128;
 __host__ __device__ __forceinline__ Splits fixed_splits(int P) {
   if (P <= 0) return {0, 0};
   int S = (P + kKeysPerSplit - 1) / kKeysPerSplit;
@@ -398,22 +398,36 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
     }
   }
   cluster_sync_all();  // every partial has arrived
+  // one warp per merged row: the split weights are formed once per row, each
+  // lane combines features lane + 32c
   const int rows = min(per, kQT - s * per);
-  for (int idx = tid; idx < rows * HD; idx += 128) {
-    const int rl = idx / HD, dd = idx % HD, v = q0 + s * per + rl;
-    if (v >= nqv) continue;
+  for (int rl = warp; rl < rows; rl += 4) {
+    const int v = q0 + s * per + rl;
+    if (v >= nqv) break;
+    float mt[kMaxSplits], w[kMaxSplits];
     float M = -INFINITY;
-    for (int t = 0; t < sp.S; ++t) M = fmaxf(M, xbuf[((size_t)t * per + rl) * XLD + HD]);
-    float acc = 0.f, l = 0.f;
-    for (int t = 0; t < sp.S; ++t) {
-      const float* x = xbuf + ((size_t)t * per + rl) * XLD;
-      const float w = exp2f(x[HD] - M);
-      acc += w * x[dd];
-      l += w * x[HD + 1];
+#pragma unroll
+    for (int t = 0; t < kMaxSplits; ++t) {
+      mt[t] = t < sp.S ? xbuf[((size_t)t * per + rl) * XLD + HD] : -INFINITY;
+      M = fmaxf(M, mt[t]);
+    }
+    float l = 0.f;
+#pragma unroll
+    for (int t = 0; t < kMaxSplits; ++t) {
+      w[t] = t < sp.S ? exp2f(mt[t] - M) : 0.f;
+      if (t < sp.S) l += w[t] * xbuf[((size_t)t * per + rl) * XLD + HD + 1];
     }
     const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
-    a.part_o[qi * HD + dd] = acc;
-    if (dd == 0) {
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      const int dd = lane + 32 * c;
+      float acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < kMaxSplits; ++t)
+        if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * XLD + dd];
+      a.part_o[qi * HD + dd] = acc;
+    }
+    if (lane == 0) {
       a.part_ml[qi * 2 + 0] = M;
       a.part_ml[qi * 2 + 1] = l;
     }
