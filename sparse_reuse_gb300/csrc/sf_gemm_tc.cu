@@ -364,9 +364,6 @@ int max_active_clusters(int s) {
   return (s >= 2 && s <= 8) ? cache[s] : 0;
 }
 
-// K splits for an M x K weight over n_tiles row tiles: the largest cluster
-// size that keeps every (m, n) tile resident in one wave and gives each CTA
-// at least one K block.
 // Prefix keys or values of one layer, [rows = R * P][nkv][hd] bf16, as a 3-D
 // TMA source with (64 dims, 1 head, 64 keys) boxes and 128-byte swizzling.
 bool make_tmap_kv(CUtensorMap* tm, const void* base, int hd, int nkv, uint64_t rows) {
@@ -381,6 +378,9 @@ bool make_tmap_kv(CUtensorMap* tm, const void* base, int hd, int nkv, uint64_t r
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K splits for an M x K weight over n_tiles row tiles: the largest cluster
+// size that keeps every (m, n) tile resident in one wave and gives each CTA
+// at least one K block.
 int gemm_tc_splits(int M, int K, int n_tiles) {
   const int m_tiles = M / tc::BM, nk = K / tc::BK, tiles = std::max(1, m_tiles * n_tiles);
   const int want = std::min(sm_count() / tiles, nk);
