@@ -81,6 +81,23 @@ def pass_work(cfg, rc_counts):
     return tot
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
+# from the committed ncu captures of the current kernels: profiles/
+# gemm_tc_1p5b_2layer.md and profiles/gemm_attn_14b_2layer.md.  A kernel
+# changed since its capture has no entry (traffic is then reported as null).
+NCU_TRAFFIC = {
+    ("1.5b", "gemm_gateup"): 55.31e6,
+    ("1.5b", "gemm_down"): 28.72e6,
+    ("1.5b", "gemm_o"): 7.52e6,
+    ("1.5b", "gemm_qkv"): 6.58e6,
+    ("14b", "gemm_gateup"): 288.35e6 + 5.67e6,
+    ("14b", "gemm_o"): 133.12e6 + 10.63e6,
+    ("14b", "gemm_down"): 148.69e6 + 3.19e6,
+    ("14b", "gemm_qkv"): 76.13e6 + 1.71e6,
+    ("14b", "attn_prefix"): 69.18e6 + 2.70e6,
+}
+
+
 # ------------------------------------------------------------------ multi-GPU replicas
 
 def replica_seed(rank: int) -> int:
@@ -394,7 +411,8 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": bytes_l / per_launch_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = NCU_TRAFFIC.get((cfg.name, dom))
+    roof["traffic_unit"] = "bytes per launch"
     roof["kernel"] = dom
     roof["peak_source"] = pk["source"]
     roof["share_of_pass"] = dom_ms / total_fam_ms if total_fam_ms else None
