@@ -61,7 +61,9 @@ def layer_work(cfg, t_rc):
     fam["gemm_down"] = dict(flops=2.0 * t_rc * d * F, bytes=d * F * wb + t_rc * F * wb + t_rc * d * 4)
     fam["attn_prefix"] = dict(flops=4.0 * t_rc * nq * hd * P, bytes=R * 2 * P * nkv * hd * wb + t_rc * nq * hd * wb)
     fam["attn_block"] = dict(flops=4.0 * T * nq * hd * L, bytes=t_rc * (nq + 2 * nkv) * hd * wb + T * nq * hd * wb)
-    fam["gate"] = dict(flops=6.0 * T * d, bytes=(2 * T + t_rc) * d * 4)
+    # gate: h and the recompute rows of f read, H written, the attention
+    # RMSNorm of the recompute rows written; norm: the FFN RMSNorm
+    fam["gate"] = dict(flops=10.0 * T * d, bytes=(2 * T + t_rc) * d * 4 + t_rc * d * wb)
     fam["norm"] = dict(flops=4.0 * t_rc * d, bytes=t_rc * d * (4 + wb))
     return fam
 

@@ -90,8 +90,9 @@ typedef struct sf_ctx sf_ctx;
  * device memory and allocates every workspace the pass needs for the given
  * capacities (no allocation happens in sf_verify).  Synchronous.
  * Errors: SF_ERR_INVALID_ARG (null), SF_ERR_UNSUPPORTED (head_dim not 64/128,
- * d_model % 128, nq % nkv, block_len > 64,
- * max_requests * max_branches > 1024, more than 8192 rows), SF_ERR_OOM,
+ * d_model % 128 or d_model > 16384, more than 1024 layers, nq % nkv,
+ * block_len > 64, max_requests * max_branches > 1024, more than 8192 rows),
+ * SF_ERR_OOM,
  * SF_ERR_CUDA.  *out is NULL on error. */
 sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_ctx** out);
 
@@ -144,8 +145,9 @@ const char* sf_last_error(const sf_ctx* ctx);
 
 /* Kernel families, for launch counting and per-family timing. */
 typedef enum sf_kernel_family {
-  SF_K_GATE = 0,        /* gate + compaction + source resolution (+ previous layer's residual) */
-  SF_K_NORM = 1,        /* RMSNorm + gather of recompute rows */
+  SF_K_GATE = 0,        /* gate + compaction + source resolution + attention RMSNorm of the
+                           recompute rows (+ previous layer's residual) */
+  SF_K_NORM = 1,        /* FFN RMSNorm + gather of recompute rows */
   SF_K_GEMM_QKV = 2,    /* packed QKV projection + rotary epilogue */
   SF_K_ATTN_PREFIX = 3, /* attention of recomputed queries over the shared prefix */
   SF_K_ATTN_BLOCK = 4,  /* block attention of every row + merge with the prefix partial */

@@ -58,7 +58,8 @@ void free_ctx(sf_ctx* c) {
     cudaFree(L.wqkv); cudaFree(L.wo); cudaFree(L.wgu); cudaFree(L.wd); cudaFree(L.g1); cudaFree(L.g2);
   }
   void* bufs[] = {c->H, c->h, c->fphys, c->xn, c->qkv, c->attn, c->u, c->y32, c->part_o, c->part_ml,
-                  c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->err_dev, c->rope};
+                  c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->epoch,
+                  c->err_dev, c->rope};
   for (void* b : bufs) cudaFree(b);
   if (c->err_host) cudaFreeHost(c->err_host);
   for (auto e : c->ev_start) cudaEventDestroy(e);
@@ -175,9 +176,13 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     ga.T = T;
     ga.d = d;
     ga.L = L;
-    if (launch_gate(lc, ga, bf16) != cudaSuccess) return lc.err;
-
-    launch_rmsnorm_gather(lc, SF_K_NORM, c->H, c->rc, c->meta, T, W.g1, s.rms_eps, c->xn, d, bf16, c->err_dev);
+    ga.xn = c->xn;
+    ga.gain = W.g1;
+    ga.eps = s.rms_eps;
+    ga.done = c->epoch + 1;
+    ga.epoch = c->epoch;
+    ga.layer = l;
+    if (launch_gate_norm(lc, ga, bf16) != cudaSuccess) return lc.err;
 
     GemmArgs g{};
     EpiArgs e{};
@@ -224,7 +229,7 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     if (run_gemm(c, lc, SF_K_GEMM_DOWN, g, &W.tm_wd, &c->tm_u, kEpiStore, e) != cudaSuccess) return lc.err;
   }
   launch_final_residual(lc, c->h, c->fphys, c->rcslot[(nl - 1) & 1], p.hidden_out, bf16,
-                        c->dbg_hidden ? c->dbg_hidden + (size_t)nl * T * d : nullptr, T, d, c->err_dev);
+                        c->dbg_hidden ? c->dbg_hidden + (size_t)nl * T * d : nullptr, T, d, c->epoch, c->err_dev);
   if (lc.err == cudaSuccess) lc.err = cudaMemcpyAsync(c->err_host, c->err_dev, sizeof(unsigned),
                                                       cudaMemcpyDeviceToHost, lc.st);
   return lc.err;
@@ -255,7 +260,8 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
       s.d_ffn <= 0 || s.block_len <= 0 || s.max_requests <= 0 || s.max_branches <= 0 || s.max_prefix < 0 ||
       !(s.rms_eps >= 0.f) || !(s.rope_theta > 0.f) || (s.dtype != SF_F32 && s.dtype != SF_BF16))
     return SF_ERR_INVALID_ARG;
-  if ((s.head_dim != 64 && s.head_dim != 128) || s.d_model % 128 != 0 || s.n_q_heads % s.n_kv_heads != 0 ||
+  if ((s.head_dim != 64 && s.head_dim != 128) || s.d_model % 128 != 0 || s.d_model > 16384 || s.n_layers > 1024 ||
+      s.n_q_heads % s.n_kv_heads != 0 ||
       s.block_len > 64 || s.max_branches > 127 || (long)s.max_requests * s.max_branches > kMaxTreeSlots ||
       (long)s.max_requests * s.max_branches * s.block_len > kMaxRows)
     return SF_ERR_UNSUPPORTED;
@@ -320,6 +326,7 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
   SF_TRY(dalloc(&c->rcslot[1], (size_t)T * 4));
   SF_TRY(dalloc(&c->meta, (size_t)(s.max_requests + 2) * 4));
   SF_TRY(dalloc(&c->ticket, 64));
+  SF_TRY(dalloc(&c->epoch, 64));
   SF_TRY(dalloc(&c->err_dev, 64));
   SF_TRY(cudaHostAlloc((void**)&c->err_host, 64, cudaHostAllocDefault));
   *c->err_host = 0;

@@ -193,6 +193,179 @@ __global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ GateA
   if (threadIdx.x == 0) *a.ticket = 0u;
 }
 
+// ---------------------------------------------------------------- fused gate
+
+// Completion tag of this layer's compaction: (pass epoch * 1024 + layer) * 2 + 1
+// is unique to this layer of this pass (at most 1024 layers) and never zero,
+// so the word needs no clearing between layers or passes.
+__device__ __forceinline__ unsigned done_tag(const GateArgs& a) {
+  return ((*a.epoch) * 1024u + (unsigned)a.layer) * 2u + 1u;
+}
+
+__device__ __forceinline__ unsigned ld_volatile_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_volatile_u32(unsigned* p, unsigned v) {
+  asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long gate_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+constexpr unsigned long long kDoneWaitNs = 2000000000ull;  // a wait that gives up raises kErrTimeout
+
+// Gate, attention RMSNorm, compaction and source resolution of one layer in
+// one launch, one CTA per row (r, i, n):
+//   1. the row's layer input H (previous layer's residual applied) and its
+//      gate decision against the parent row;
+//   2. the CTA that takes the last ticket compacts and resolves every row
+//      (compact_and_resolve) and then sets the layer's completion tag;
+//   3. a recompute row's CTA waits for that tag, reads its slot and writes its
+//      normalised row there (folded rows' CTAs leave after step 1).
+// Only CTAs that already took a ticket wait, and they wait for the CTA that
+// took the last one, so the wait always ends; it is bounded all the same.
+// Short rows (VEC > 0) stay in registers; long rows (VEC == 0) are kept in
+// dynamic shared memory until their slot is known.
+template <bool kLayer0, typename TIn, int VEC, typename TAct>
+__global__ void __launch_bounds__(256) gate_norm_kernel(const __grid_constant__ GateArgs a) {
+  __shared__ float red[32];
+  __shared__ int tmp[32];
+  __shared__ int s_fold, s_last, s_slot;
+  extern __shared__ __align__(16) unsigned char dyn[];
+  pdl_wait();
+  pdl_trigger();
+
+  const int row = blockIdx.x;
+  const int L = a.L, Bp = a.tree.Bp;
+  const int n = row % L, rb = row / L, i = rb % Bp, r = rb / Bp;
+  const int prow = i > 0 ? (r * Bp + a.tree.parent[r * Bp + i]) * L + n : -1;
+  const int d4 = a.d >> 2;
+  float4* xrow = reinterpret_cast<float4*>(dyn);
+  unsigned char* cscratch = dyn + (VEC > 0 ? 0 : (size_t)a.d * sizeof(float));  // compaction's shared memory
+
+  float diff2 = 0.f, par2 = 0.f, ss = 0.f;
+  float4 xs[VEC > 0 ? VEC : 1];
+  if constexpr (VEC > 0) {
+    float4 ys[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * blockDim.x;
+      if (c < d4) {
+        xs[k] = layer_input4<kLayer0, TIn>(a, row, c);
+        if (prow >= 0) ys[k] = layer_input4<kLayer0, TIn>(a, prow, c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * blockDim.x;
+      if (c < d4) {
+        const float4 x = xs[k];
+        *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
+        if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
+        ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+        if (prow >= 0) {
+          const float4 y = ys[k];
+          const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
+          diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
+          par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+        }
+      }
+    }
+  } else {
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+      const float4 x = layer_input4<kLayer0, TIn>(a, row, c);
+      *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
+      if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
+      xrow[c] = x;
+      ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+      if (prow >= 0) {
+        const float4 y = layer_input4<kLayer0, TIn>(a, prow, c);
+        const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
+        diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
+        par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+      }
+    }
+  }
+  if (prow >= 0) {
+    diff2 = block_sum(diff2, red);
+    par2 = block_sum(par2, red);
+  }
+  ss = block_sum(ss, red);
+  if (threadIdx.x == 0) {
+    // rho <= delta  <=>  ||diff||^2 <= delta^2 ||parent||^2 (covers a zero parent)
+    const int f = (prow >= 0 && a.delta > 0.f && diff2 <= a.delta * a.delta * par2) ? 1 : 0;
+    a.fold[row] = (uint8_t)f;
+    if (a.fold_user) a.fold_user[row] = (uint8_t)f;
+    s_fold = f;
+    // only the flag has to be visible before this block's ticket is counted
+    __threadfence();
+    s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  const int f = s_fold;
+  const unsigned tag = done_tag(a);
+  if (s_last) {
+    __threadfence();
+    uint8_t* flags = cscratch;
+    int* slot = reinterpret_cast<int*>(cscratch + ((a.T + 15) & ~15));
+    compact_and_resolve(a, flags, slot, tmp);
+    // every write of the compaction is visible before the tag
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      *a.ticket = 0u;
+      s_slot = slot[row];
+      __threadfence();
+      st_volatile_u32(a.done, tag);
+    }
+    __syncthreads();
+  } else {
+    if (f) return;
+    if (threadIdx.x == 0) {
+      unsigned long long t0 = 0;
+      while (ld_volatile_u32(a.done) != tag) {
+        const unsigned long long t = gate_timer_ns();
+        if (t0 == 0) t0 = t;
+        if (t - t0 > kDoneWaitNs) {
+          raise_error(a.err, kErrTimeout);
+          break;
+        }
+        __nanosleep(64);
+      }
+      __threadfence();
+      s_slot = __ldcg(a.rcslot + row);  // a recompute row is its own source
+    }
+    __syncthreads();
+  }
+  if (f) return;
+  const int sl = s_slot;
+  const float rstd = rsqrtf(ss / (float)a.d + a.eps);
+  TAct* out = reinterpret_cast<TAct*>(a.xn) + (size_t)sl * a.d;
+  if constexpr (VEC > 0) {
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * blockDim.x;
+      if (c < d4) {
+        const float4 v = xs[k];
+        const float4 w = *reinterpret_cast<const float4*>(a.gain + c * 4);
+        store4<TAct>(out + c * 4, make_float4(v.x * rstd * w.x, v.y * rstd * w.y, v.z * rstd * w.z, v.w * rstd * w.w));
+      }
+    }
+  } else {
+    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+      const float4 v = xrow[c];
+      const float4 w = *reinterpret_cast<const float4*>(a.gain + c * 4);
+      store4<TAct>(out + c * 4, make_float4(v.x * rstd * w.x, v.y * rstd * w.y, v.z * rstd * w.z, v.w * rstd * w.w));
+    }
+  }
+}
+
 // RMSNorm of rows rc[g] (or g when rc is null), g < count, gathered into a
 // dense [count][d] activation matrix.
 template <typename TAct>
@@ -230,9 +403,12 @@ __global__ void __launch_bounds__(256) rmsnorm_gather_kernel(const float* X, con
 // Last layer's residual add for every row, cast to the output type.
 template <typename TOut>
 __global__ void __launch_bounds__(256) final_residual_kernel(const float* h, const float* f, const int32_t* rcslot,
-                                                             TOut* out, float* dbg, int T, int d, unsigned* err) {
+                                                             TOut* out, float* dbg, int T, int d, unsigned* epoch,
+                                                             unsigned* err) {
   pdl_wait();
   pdl_trigger();
+  // every gate of this pass has completed: the next pass tags its decisions anew
+  if (epoch && blockIdx.x == 0 && threadIdx.x == 0) *epoch += 1u;
   const int d4 = d >> 2;
   for (int row = blockIdx.x; row < T; row += gridDim.x) {
     int s = rcslot[row];
@@ -306,6 +482,38 @@ cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16) {
   return lc.err;
 }
 
+namespace {
+
+template <int VEC, typename TAct>
+cudaError_t launch_gate_norm_vec(Launch& lc, const GateArgs& a, int bf16) {
+  // the long row (VEC == 0), then the compaction's flags and slots
+  const size_t dyn =
+      (VEC > 0 ? 0 : (size_t)a.d * sizeof(float)) + (size_t)((a.T + 15) & ~15) + (size_t)a.T * sizeof(int);
+  auto k0 = a.x_in == nullptr ? gate_norm_kernel<false, float, VEC, TAct>
+                              : (bf16 ? gate_norm_kernel<true, __nv_bfloat16, VEC, TAct>
+                                      : gate_norm_kernel<true, float, VEC, TAct>);
+  if (dyn > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(lc.st, dim3(a.T), dim3(256), dyn, 1, k0, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gate_norm(Launch& lc, const GateArgs& a, int bf16) {
+  if (a.d % 4 != 0 || !a.xn || !a.gain || !a.done || !a.epoch || !a.ticket) return lc.err = cudaErrorInvalidValue;
+  const int d4 = a.d / 4;
+  lc.before(SF_K_GATE);
+  if (bf16)
+    lc.check(d4 <= 512 ? launch_gate_norm_vec<2, __nv_bfloat16>(lc, a, bf16)
+                       : launch_gate_norm_vec<0, __nv_bfloat16>(lc, a, bf16));
+  else
+    lc.check(d4 <= 512 ? launch_gate_norm_vec<2, float>(lc, a, bf16) : launch_gate_norm_vec<0, float>(lc, a, bf16));
+  lc.after(SF_K_GATE);
+  return lc.err;
+}
+
 cudaError_t launch_rmsnorm_gather(Launch& lc, int fam, const float* X, const int32_t* rc, const int32_t* count,
                                   int max_rows, const float* gain, float eps, void* out, int d, int act_bf16,
                                   unsigned* err) {
@@ -322,15 +530,15 @@ cudaError_t launch_rmsnorm_gather(Launch& lc, int fam, const float* X, const int
 }
 
 cudaError_t launch_final_residual(Launch& lc, const float* h, const float* f, const int32_t* rcslot, void* out,
-                                  int out_bf16, float* dbg, int T, int d, unsigned* err) {
+                                  int out_bf16, float* dbg, int T, int d, unsigned* epoch, unsigned* err) {
   lc.before(SF_K_RESIDUAL);
   const int grid = grid_rows(T);
   if (out_bf16)
     lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, final_residual_kernel<__nv_bfloat16>, h, f, rcslot,
-                        (__nv_bfloat16*)out, dbg, T, d, err));
+                        (__nv_bfloat16*)out, dbg, T, d, epoch, err));
   else
     lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, final_residual_kernel<float>, h, f, rcslot, (float*)out,
-                        dbg, T, d, err));
+                        dbg, T, d, epoch, err));
   lc.after(SF_K_RESIDUAL);
   return lc.err;
 }

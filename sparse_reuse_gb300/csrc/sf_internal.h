@@ -72,6 +72,7 @@ struct sf_ctx {
   int32_t* rcslot[2] = {nullptr, nullptr};  // [T_max], ping-pong between layers
   int32_t* meta = nullptr;  // [0] = rc count, [1 + r] = first recompute slot of request r
   unsigned* ticket = nullptr;
+  unsigned* epoch = nullptr;  // [0] pass counter, [1] completion tag of the gate's compaction
   unsigned* err_dev = nullptr;
   unsigned* err_host = nullptr;  // pinned mirror, refreshed at the end of every pass
   float2* rope = nullptr;   // [max_pos][hd/2] (cos, sin), computed in double on the host
@@ -159,6 +160,13 @@ struct GateArgs {
   float delta;
   int T, d, L;
   Tree tree;
+  // fused gate + attention RMSNorm (gate_norm_kernel) only
+  void* xn;               // [T_rc][d] context dtype: normalised recompute rows
+  const float* gain;      // [d] attention RMSNorm gain
+  float eps;
+  unsigned* done;         // completion tag of the layer's compaction
+  const unsigned* epoch;  // pass counter, advanced by the final residual kernel
+  int layer;
 };
 
 // sf_gate.cu
@@ -166,8 +174,10 @@ cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16);
 cudaError_t launch_rmsnorm_gather(Launch& lc, int fam, const float* X, const int32_t* rc,
                                   const int32_t* count, int max_rows, const float* gain, float eps,
                                   void* out, int d, int act_bf16, unsigned* err);
+cudaError_t launch_gate_norm(Launch& lc, const GateArgs& a, int bf16);
 cudaError_t launch_final_residual(Launch& lc, const float* h, const float* f, const int32_t* rcslot,
-                                  void* out, int out_bf16, float* dbg, int T, int d, unsigned* err);
+                                  void* out, int out_bf16, float* dbg, int T, int d, unsigned* epoch,
+                                  unsigned* err);
 cudaError_t launch_pack_transpose(cudaStream_t st, const void* src, int K, int N, void* dst, int ld_dst,
                                   int row_base, int interleave, int bf16);
 
