@@ -62,9 +62,11 @@ __device__ int block_exclusive_scan(int v, int* tmp, int* total) {
   return base + x - v;
 }
 
-// Compaction (stable, ascending row id) and source resolution; run by the
-// last thread block of the gate kernel once every fold flag is in memory.
-__device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot, int* tmp) {
+// Compaction (stable, ascending row id): the recompute list, the slot of every
+// recompute row (its own source slot) and the per-request offsets.  Run by the
+// last thread block of the gate kernel once every fold flag is in memory;
+// slot[] (shared) receives each row's slot, -1 for a folded row.
+__device__ void compact(const GateArgs& a, uint8_t* flags, int* slot, int* tmp) {
   const int T = a.T, L = a.L, Bp = a.tree.Bp, R = a.tree.R;
   for (int row = threadIdx.x; row < T; row += blockDim.x) flags[row] = __ldcg(a.fold + row);
   __syncthreads();
@@ -78,6 +80,7 @@ __device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot
     if (!flags[row]) {
       slot[row] = s;
       a.rc[s] = row;
+      a.rcslot[row] = s;
       if (a.rc_user) a.rc_user[s] = row;
       ++s;
     } else {
@@ -85,6 +88,18 @@ __device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    a.meta[0] = total;
+    for (int r = 0; r < R; ++r) a.meta[1 + r] = slot[r * Bp * L];  // main row n = 0 always recomputes
+    a.meta[1 + R] = total;
+    if (a.rc_count_user) *a.rc_count_user = total;
+  }
+}
+
+// Source resolution of the folded rows (a folded (i, n) follows its chain to
+// the nearest ancestor that recomputed n) and every row's source branch.
+__device__ void resolve(const GateArgs& a, const uint8_t* flags, const int* slot) {
+  const int T = a.T, L = a.L, Bp = a.tree.Bp;
   for (int row = threadIdx.x; row < T; row += blockDim.x) {
     const int n = row % L, rb = row / L, i = rb % Bp, r = rb / Bp;
     int b = i, steps = 0;
@@ -96,17 +111,18 @@ __device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot
         break;
       }
     }
-    const int sl = slot[(r * Bp + b) * L + n];
-    if (sl < 0) raise_error(a.err, kErrGate);
-    a.rcslot[row] = sl < 0 ? 0 : sl;
+    if (b != i) {
+      const int sl = slot[(r * Bp + b) * L + n];
+      if (sl < 0) raise_error(a.err, kErrGate);
+      a.rcslot[row] = sl < 0 ? 0 : sl;
+    }
     if (a.src_user) a.src_user[row] = b;
   }
-  if (threadIdx.x == 0) {
-    a.meta[0] = total;
-    for (int r = 0; r < R; ++r) a.meta[1 + r] = slot[r * Bp * L];  // main row n = 0 always recomputes
-    a.meta[1 + R] = total;
-    if (a.rc_count_user) *a.rc_count_user = total;
-  }
+}
+
+__device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot, int* tmp) {
+  compact(a, flags, slot, tmp);
+  resolve(a, flags, slot);
 }
 
 // One block per row (r, i, n): the row's layer input H (previous layer's
@@ -202,14 +218,20 @@ __device__ __forceinline__ unsigned done_tag(const GateArgs& a) {
   return ((*a.epoch) * 1024u + (unsigned)a.layer) * 2u + 1u;
 }
 
-__device__ __forceinline__ unsigned ld_volatile_u32(const unsigned* p) {
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_volatile_u32(unsigned* p, unsigned v) {
-  asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ unsigned long long gate_timer_ns() {
@@ -303,42 +325,40 @@ __global__ void __launch_bounds__(256) gate_norm_kernel(const __grid_constant__ 
     a.fold[row] = (uint8_t)f;
     if (a.fold_user) a.fold_user[row] = (uint8_t)f;
     s_fold = f;
-    // only the flag has to be visible before this block's ticket is counted
-    __threadfence();
-    s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+    // the ticket releases the flag to the CTA that takes the last one, which
+    // acquires every earlier ticket's flag
+    s_last = atom_add_acq_rel_gpu(a.ticket, 1u) == gridDim.x - 1;
   }
   __syncthreads();
   const int f = s_fold;
   const unsigned tag = done_tag(a);
   if (s_last) {
-    __threadfence();
     uint8_t* flags = cscratch;
     int* slot = reinterpret_cast<int*>(cscratch + ((a.T + 15) & ~15));
-    compact_and_resolve(a, flags, slot, tmp);
-    // every write of the compaction is visible before the tag
-    __threadfence();
-    __syncthreads();
+    compact(a, flags, slot, tmp);
     if (threadIdx.x == 0) {
       *a.ticket = 0u;
       s_slot = slot[row];
-      __threadfence();
-      st_volatile_u32(a.done, tag);
+      // after compact's closing block barrier this release covers every
+      // thread's writes of the list, the recompute rows' slots and the offsets
+      st_release_gpu(a.done, tag);
     }
+    // the folded rows' sources are resolved while the recompute rows write
+    resolve(a, flags, slot);
     __syncthreads();
   } else {
     if (f) return;
     if (threadIdx.x == 0) {
       unsigned long long t0 = 0;
-      while (ld_volatile_u32(a.done) != tag) {
+      while (ld_acquire_gpu(a.done) != tag) {
         const unsigned long long t = gate_timer_ns();
         if (t0 == 0) t0 = t;
         if (t - t0 > kDoneWaitNs) {
           raise_error(a.err, kErrTimeout);
           break;
         }
-        __nanosleep(64);
+        __nanosleep(32);
       }
-      __threadfence();
       s_slot = __ldcg(a.rcslot + row);  // a recompute row is its own source
     }
     __syncthreads();
