@@ -448,7 +448,6 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   bf16* sK = sQ + kBQT * LD;
   bf16* sV = sK + kKB * LD;
-  float* sP = reinterpret_cast<float*>(sV + kKB * LD);  // [kBQT][HD] merged prefix outputs
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rb = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;  // rb = r * Bp + i
   const int G = a.nq / a.nkv, L = a.L;
@@ -493,28 +492,24 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   pdl_wait();
   pdl_trigger();
   if (a.P == 0) load_rows();
-  // the merged prefix state of each query (previous kernel), needed only
-  // after the block part: its output rows are copied while that runs
+  // the merged prefix state of this thread's two query vectors (previous
+  // kernel), needed only after the block part: loaded into registers while it
+  // runs
   float mp[2] = {0.f, 0.f}, lp[2] = {0.f, 0.f};
+  float2 pp[2][HD / 8];
   if (a.P > 0) {
-    for (int idx = tid; idx < kBQT * (HD / 4); idx += 64) {
-      const int row = idx / (HD / 4), c4 = idx % (HD / 4), v = q0 + row;
-      const bool ok = v < nqv;
-      const size_t qi = (size_t)slot[ok ? v / G : 0] * a.nq + kvh * G + (ok ? v % G : 0);
-      cp_async16(sP + row * HD + c4 * 4, a.part_o + qi * HD + c4 * 4, ok);
-    }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
-      if (v < nqv) {
-        const size_t qi = (size_t)slot[v / G] * a.nq + kvh * G + v % G;
-        mp[half] = a.part_ml[qi * 2];
-        lp[half] = a.part_ml[qi * 2 + 1];
-      }
+      const size_t qi = v < nqv ? (size_t)slot[v / G] * a.nq + kvh * G + v % G : (size_t)slot[0] * a.nq + kvh * G;
+      const float* po = a.part_o + qi * HD + (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < HD / 8; ++nt) pp[half][nt] = *reinterpret_cast<const float2*>(po + nt * 8);
+      mp[half] = a.part_ml[qi * 2];
+      lp[half] = a.part_ml[qi * 2 + 1];
     }
   }
-  cp_async_commit();
-  cp_async_wait<1>();  // the projected rows have landed
+  cp_async_wait<0>();  // the projected rows have landed
   __syncthreads();
   uint32_t qf[HD / 16][4];
   load_q_frags<HD>(qf, sQ, warp, lane);
@@ -547,8 +542,6 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
 #pragma unroll
   for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   pv_accum<HD>(o, sc, sV, lane);
-  cp_async_wait<0>();  // the prefix outputs have landed
-  __syncthreads();
 
   bf16* out = reinterpret_cast<bf16*>(a.attn);
 #pragma unroll
@@ -561,18 +554,14 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
     float l, wb;
     if (a.P > 0) {
       // merge with the prefix state of this query (one per recompute slot and head)
-      float2 pp[HD / 8];
-      const float* po = sP + (v - q0) * HD + (lane & 3) * 2;
-#pragma unroll
-      for (int nt = 0; nt < HD / 8; ++nt) pp[nt] = *reinterpret_cast<const float2*>(po + nt * 8);
       const float M = fmaxf(mb, mp[half]);
       wb = exp2f(mb - M);
       const float wp = exp2f(mp[half] - M);
       l = lb * wb + lp[half] * wp;
 #pragma unroll
       for (int nt = 0; nt < HD / 8; ++nt) {
-        acc[nt][0] = o[nt][2 * half] * wb + wp * pp[nt].x;
-        acc[nt][1] = o[nt][2 * half + 1] * wb + wp * pp[nt].y;
+        acc[nt][0] = o[nt][2 * half] * wb + wp * pp[half][nt].x;
+        acc[nt][1] = o[nt][2 * half + 1] * wb + wp * pp[half][nt].y;
       }
     } else {
       l = lb;
@@ -717,13 +706,13 @@ template <int HD>
 cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   constexpr int LD = HD + 8;
   const int G = a.nq / a.nkv;
-  const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16) + (size_t)kBQT * HD * sizeof(float);
+  const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16);
   static cudaError_t attr = [&] {
     cudaError_t e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          prefix_smem_bytes<HD>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)((kBQT + 2 * kKB) * LD * sizeof(bf16) + kBQT * HD * sizeof(float)));
+                               (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
     return e;
   }();
   if (attr != cudaSuccess) return lc.err = attr;
