@@ -434,6 +434,372 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   }
 }
 
+// ------------------------------------------------------------ tcgen05 prefix path
+//
+// Prefix partials on the 5th-generation tensor cores: CTA = (128 query vectors
+// of one request and KV head = the 128 TMEM lanes, one split of the prefix).
+// Per block of 64 keys:
+//   S = Q K^T       tcgen05.mma, Q and K K-major in shared memory, S in TMEM
+//                   (two buffers, so the next block's scores overlap this
+//                   block's softmax);
+//   P = exp2(S - m) by the softmax warps, one query row per thread, written as
+//                   bf16 to shared memory (K-major, 128-byte swizzle);
+//   O += P V        tcgen05.mma, V MN-major as the TMA box leaves it, O in TMEM.
+// The running max m of a row only moves when a block's max exceeds it by more
+// than 2^8, and O is then rescaled in TMEM; the partial state (m, l, O) stays
+// exact because m is whatever reference the exponentials used.
+// Warp 0 streams K and V through two kTcStages-deep rings of TMA loads (lane 0
+// the keys, freed once their scores are computed; lane 1 the values, freed
+// once P V is done), warp 1 owns TMEM and issues the MMAs, warps 2-5 load Q and
+// run the softmax and the epilogue.
+// The split CTAs of a tile form a cluster and merge as the CUDA-core path does.
+constexpr int kTcQ = 128;
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;
+constexpr int kTcMinKeysPerSplit = 512;
+constexpr int kTcMaxSplits = 4;
+// Prefixes of at least this many keys take the tcgen05 kernel; shorter ones
+// the mma.sync kernel, whose smaller fixed cost per CTA wins there.
+constexpr int kTcMinPrefix = 2048;
+constexpr float kTcRescaleLog2 = 8.f;
+
+// Few long splits: the fixed cost of a CTA (TMEM, barriers, the first scores,
+// the epilogue) is paid once per split.
+__host__ __device__ __forceinline__ Splits tc_splits(int P) {
+  if (P <= 0) return {0, 0};
+  int S = (P + kTcMinKeysPerSplit - 1) / kTcMinKeysPerSplit;
+  S = S < 1 ? 1 : (S > kTcMaxSplits ? kTcMaxSplits : S);
+  const int len = (((P + S - 1) / S) + kKB - 1) / kKB * kKB;
+  return {(P + len - 1) / len, len};
+}
+
+template <int HD>
+struct TcLayout {
+  static constexpr int QH = HD / 64;                    // 64-dim halves
+  static constexpr int HALF = kTcQ * 128;               // one 64-dim half of Q: 128 rows x 128 B
+  static constexpr int KV_TILE = kKB * 128;             // one 64-dim half of a K or V block
+  static constexpr int STAGE = QH * KV_TILE;            // K (or V) of one block
+  static constexpr int P_TILE = kTcQ * 128;             // P: 128 rows x 64 keys (bf16)
+  static constexpr int OFF_K = QH * HALF;
+  static constexpr int OFF_V = OFF_K + kTcStages * STAGE;
+  static constexpr int OFF_P = OFF_V + kTcStages * STAGE;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
+  static constexpr int BYTES = OFF_BAR + 256 + 1024;   // + alignment of the dynamic window
+  static constexpr int XLD = HD + 4;                    // merge exchange row: o[HD], m, l (16-byte rows)
+  static constexpr int TMEM_COLS = 256;                 // S0 [0,64), S1 [64,128), O [128, 128 + HD)
+  static_assert((kTcQ + kMaxSplits - 1) * XLD * 4 <= OFF_P, "merge exchange area");
+};
+
+__device__ __forceinline__ void tmem_ld32_raw(uint32_t taddr, float (&v)[32]) { tc::tmem_ld32(taddr, v); }
+
+// 64 consecutive fp32 columns of this warp's 32 TMEM lanes, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]), "=r"(r[32 * h + 4]),
+          "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]), "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]),
+          "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]), "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]),
+          "=r"(r[32 * h + 14]), "=r"(r[32 * h + 15]), "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]),
+          "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]), "=r"(r[32 * h + 20]), "=r"(r[32 * h + 21]),
+          "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]), "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]),
+          "=r"(r[32 * h + 26]), "=r"(r[32 * h + 27]), "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]),
+          "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+        : "r"(taddr + 32 * h));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_constant__ CUtensorMap tmK,
+                                                                const __grid_constant__ CUtensorMap tmV,
+                                                                const AttnArgs a) {
+  using Lay = TcLayout<HD>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  unsigned char* sQ = base;
+  unsigned char* sK = base + Lay::OFF_K;
+  unsigned char* sV = base + Lay::OFF_V;
+  unsigned char* sP = base + Lay::OFF_P;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + Lay::OFF_BAR);
+  uint64_t* kfull = bar;                   // [kTcStages] K landed
+  uint64_t* vfull = bar + kTcStages;       // [kTcStages] V landed
+  uint64_t* kempty = bar + 2 * kTcStages;  // [kTcStages] K consumed by S = Q K^T
+  uint64_t* vempty = bar + 3 * kTcStages;  // [kTcStages] V consumed by O += P V
+  uint64_t* sfull = bar + 4 * kTcStages;   // [2] scores in TMEM
+  uint64_t* sempty = sfull + 2;            // [2] scores read
+  uint64_t* pfull = sempty + 2;            // [2] P written
+  uint64_t* pvdone = pfull + 2;            // [2] P V of that buffer done
+  uint64_t* qready = pvdone + 2;
+  uint64_t* ofull = qready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
+  float* xbuf = reinterpret_cast<float*>(base);  // merge exchange, over Q and the ring once they are dead
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
+  const Splits sp = tc_splits(a.P);
+  const int G = a.nq / a.nkv;
+  // recompute offsets from the gate kernel (complete once this grid runs), past L1
+  const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
+  const int q0 = blockIdx.x * kTcQ;
+  if (q0 >= nqv) {  // uniform over the cluster
+    pdl_wait();
+    return;
+  }
+  const int s = sp.S > 1 ? (int)tc::cluster_ctarank() : 0;
+  const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
+  const int nblk = (k_hi - k_lo + kKB - 1) / kKB;
+
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      tc::mbar_init(&kfull[i], 1);
+      tc::mbar_init(&vfull[i], 1);
+      tc::mbar_init(&kempty[i], 1);
+      tc::mbar_init(&vempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sfull[i], 1);
+      tc::mbar_init(&sempty[i], 128);
+      tc::mbar_init(&pfull[i], 128);
+      tc::mbar_init(&pvdone[i], 1);
+    }
+    tc::mbar_init(qready, 128);
+    tc::mbar_init(ofull, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, Lay::TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  // warp 0: lane 0 loads key block b into K stage b % kTcStages, lane 1 the
+  // value block into the V ring
+  auto issue = [&](int b, bool keys) {
+    const int st = b % kTcStages;
+    unsigned char* dst = (keys ? sK : sV) + st * Lay::STAGE;
+    uint64_t* full = keys ? &kfull[st] : &vfull[st];
+    const int z = r * a.P + k_lo + b * kKB;
+    tc::mbar_expect_tx(full, Lay::QH * Lay::KV_TILE);
+#pragma unroll
+    for (int h = 0; h < Lay::QH; ++h) tc::tma_load_3d(dst + h * Lay::KV_TILE, keys ? &tmK : &tmV, h * 64, kvh, z, full);
+  };
+  // the prefix keys and values are inputs of the pass
+  if (warp == 0 && lane < 2)
+    for (int b = 0; b < min(kTcStages, nblk); ++b) issue(b, lane == 0);
+  pdl_wait();
+  pdl_trigger();
+
+  const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
+  if (warp == 0) {
+    if (lane < 2) {
+      const bool keys = lane == 0;
+      for (int b = kTcStages; b < nblk; ++b) {
+        // the stage is free once the MMA that read block b - kTcStages has completed
+        tc::mbar_wait(keys ? &kempty[b % kTcStages] : &vempty[b % kTcStages], ((b / kTcStages) - 1) & 1, a.err);
+        issue(b, keys);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc_s = tc::idesc_bf16_f32(kTcQ, kKB);
+      const uint32_t idesc_pv = tc::idesc_bf16_f32(kTcQ, HD) | (1u << 16);  // V is MN-major
+      tc::mbar_wait(qready, 0, a.err);
+      for (int b = 0; b <= nblk; ++b) {
+        if (b < nblk) {  // S(b) = Q K(b)^T into TMEM buffer b % 2
+          const int st = b % kTcStages, sb = b & 1;
+          tc::mbar_wait(&kfull[st], (b / kTcStages) & 1, a.err);
+          if (b >= 2) tc::mbar_wait(&sempty[sb], ((b >> 1) - 1) & 1, a.err);
+          tc::fence_after_sync();
+          const unsigned char* sk = sK + st * Lay::STAGE;
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint64_t dq = tc::sw128_kmajor_desc(smem_addr(sQ + (kk >> 2) * Lay::HALF + (kk & 3) * 32));
+            const uint64_t dk = tc::sw128_kmajor_desc(smem_addr(sk + (kk >> 2) * Lay::KV_TILE + (kk & 3) * 32));
+            tc::mma_bf16(tmem + sb * kKB, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&sfull[sb]);
+          tc::mma_commit(&kempty[st]);
+        }
+        if (b >= 1) {  // O += P(j) V(j), j = b - 1
+          const int j = b - 1, st = j % kTcStages, pb = j & 1;
+          tc::mbar_wait(&pfull[pb], (j >> 1) & 1, a.err);
+          tc::mbar_wait(&vfull[st], (j / kTcStages) & 1, a.err);
+          tc::fence_after_sync();
+          const unsigned char* sv = sV + st * Lay::STAGE;
+#pragma unroll
+          for (int kk = 0; kk < kKB / 16; ++kk) {
+            const uint64_t dp = tc::sw128_kmajor_desc(smem_addr(sP + pb * Lay::P_TILE + kk * 32));
+            const uint64_t dv = tc::sw128_mnmajor_desc(smem_addr(sv + kk * 2048), Lay::KV_TILE);
+            tc::mma_bf16(tmem + 2 * kKB, dp, dv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&pvdone[pb]);
+          tc::mma_commit(&vempty[st]);
+        }
+      }
+      tc::mma_commit(ofull);
+    }
+    __syncwarp();
+  } else {
+    // softmax warps: TMEM lanes 32 * (warp % 4) .. + 31, one query row per thread
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int v = q0 + row;
+    {
+      const bool ok = v < nqv;
+      const int g = off_r + (ok ? v / G : 0), h = kvh * G + (ok ? v % G : 0);
+      const bf16* src = qkv + (size_t)g * a.ld_qkv + h * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 8; ++c)
+        cp_async16(sQ + (c >> 3) * Lay::HALF + row * 128 + (((c & 7) ^ (row & 7)) << 4), src + c * 8, ok);
+      cp_async_commit();
+      cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(qready);
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    for (int b = 0; b < nblk; ++b) {
+      const int sb = b & 1;
+      tc::mbar_wait(&sfull[sb], (b >> 1) & 1, a.err);
+      tc::fence_after_sync();
+      float sc[kKB];
+      tmem_ld64(tl + sb * kKB, sc);
+      tc::fence_before_sync();
+      tc::mbar_arrive(&sempty[sb]);
+      const int kb0 = k_lo + b * kKB;
+      float mb = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) {
+        sc[k] = kb0 + k < k_hi ? sc[k] * a.scale_log2 : -INFINITY;
+        mb = fmaxf(mb, sc[k]);
+      }
+      if (b == 0) {
+        m_ref = mb;
+      } else {
+        const bool need = mb > m_ref + kTcRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {  // warp-wide: the TMEM accesses are collective
+          const float m_new = need ? mb : m_ref;
+          const float f = exp2f(m_ref - m_new);
+          // O holds every block before b once P V of block b - 1 is done
+          tc::mbar_wait(&pvdone[(b - 1) & 1], ((b - 1) >> 1) & 1, a.err);
+          tc::fence_after_sync();
+#pragma unroll
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            float o[32];
+            tmem_ld32_raw(tl + 2 * kKB + c0, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tc::tmem_st32(tl + 2 * kKB + c0, o);
+          }
+          tc::tmem_wait_st();
+          l *= f;
+          m_ref = m_new;
+        }
+      }
+      float ls = 0.f;
+      uint32_t pk[kKB / 2];
+#pragma unroll
+      for (int k = 0; k < kKB; k += 2) {
+        const float p0 = exp2f(sc[k] - m_ref), p1 = exp2f(sc[k + 1] - m_ref);
+        ls += p0 + p1;
+        pk[k / 2] = pack_bf16(p0, p1);
+      }
+      l += ls;
+      // P buffer sb is free once P V of block b - 2 is done
+      if (b >= 2) tc::mbar_wait(&pvdone[sb], ((b - 2) >> 1) & 1, a.err);
+      unsigned char* prow = sP + sb * Lay::P_TILE + row * 128;
+#pragma unroll
+      for (int c = 0; c < kKB / 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&pfull[sb]);
+    }
+    tc::mbar_wait(ofull, 0, a.err);
+    tc::fence_after_sync();
+    float o[HD];
+#pragma unroll
+    for (int c0 = 0; c0 < HD; c0 += 32) tmem_ld32_raw(tl + 2 * kKB + c0, *reinterpret_cast<float(*)[32]>(o + c0));
+    if (sp.S == 1) {  // a single split: the partial is already the merged state
+      if (v < nqv) {
+        const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+        float* po = a.part_o + qi * HD;
+#pragma unroll
+        for (int c = 0; c < HD; c += 4) *reinterpret_cast<float4*>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        a.part_ml[qi * 2 + 0] = m_ref;
+        a.part_ml[qi * 2 + 1] = l;
+      }
+    } else {
+      // rows [rank * per, (rank + 1) * per) of the tile are merged by `rank`
+      const int per = (kTcQ + sp.S - 1) / sp.S;
+      // (the exchange area covers Q and the ring: wait until every split is past its loop)
+      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+      const int owner = row / per;
+      const uint32_t dst =
+          tc::map_to_rank(smem_addr(xbuf + ((size_t)s * per + (row - owner * per)) * Lay::XLD), (uint32_t)owner);
+#pragma unroll
+      for (int c = 0; c < HD; c += 4)
+        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + c * 4), "f"(o[c]), "f"(o[c + 1]),
+                     "f"(o[c + 2]), "f"(o[c + 3])
+                     : "memory");
+      asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(dst + HD * 4), "f"(m_ref), "f"(l) : "memory");
+    }
+  }
+  if (sp.S > 1) {
+    if (warp < 2)  // the producer and MMA warps take part in the cluster barriers too
+      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    // merge: one warp per row (warps 0-5), split weights formed once per row
+    const int rows = min((kTcQ + sp.S - 1) / sp.S, kTcQ - s * ((kTcQ + sp.S - 1) / sp.S));
+    const int per = (kTcQ + sp.S - 1) / sp.S;
+    for (int rl = warp; rl < rows; rl += kTcThreads / 32) {
+      const int v = q0 + s * per + rl;
+      if (v >= nqv) break;
+      float mt[kMaxSplits], w[kMaxSplits];
+      float M = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kMaxSplits; ++t) {
+        mt[t] = t < sp.S ? xbuf[((size_t)t * per + rl) * Lay::XLD + HD] : -INFINITY;
+        M = fmaxf(M, mt[t]);
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int t = 0; t < kMaxSplits; ++t) {
+        w[t] = t < sp.S ? exp2f(mt[t] - M) : 0.f;
+        if (t < sp.S) lsum += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + HD + 1];
+      }
+      const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        const int dd = lane + 32 * c;
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 0; t < kMaxSplits; ++t)
+          if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + dd];
+        a.part_o[qi * HD + dd] = acc;
+      }
+      if (lane == 0) {
+        a.part_ml[qi * 2 + 0] = M;
+        a.part_ml[qi * 2 + 1] = lsum;
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, Lay::TMEM_COLS);
+  }
+}
+
 // Block attention + merge: CTA = (32 query vectors of one branch and KV head,
 // two warps).  Query vector v is block position n = v / G with query head
 // kvh * G + v % G; its query is the one of the row's resolved source; its
@@ -708,8 +1074,11 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   const int G = a.nq / a.nkv;
   const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16);
   static cudaError_t attr = [&] {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         prefix_smem_bytes<HD>());
+    cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TcLayout<HD>::BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               prefix_smem_bytes<HD>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
@@ -722,11 +1091,18 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
         !make_tmap_kv(&tmV, a.pv, HD, a.nkv, (uint64_t)a.R * a.P))
       return lc.err = cudaErrorInvalidValue;
     // worst case: every row of a request recomputes
-    const Splits sp = fixed_splits(a.P);
-    dim3 grid((a.Bp * a.L * G + kQT - 1) / kQT, a.R * a.nkv, sp.S);
     lc.before(SF_K_ATTN_PREFIX);
-    lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD>(), sp.S, attn_prefix_mma<HD>, tmK,
-                        tmV, a));
+    if (a.P >= kTcMinPrefix) {
+      const Splits sp = tc_splits(a.P);
+      dim3 grid((a.Bp * a.L * G + kTcQ - 1) / kTcQ, a.R * a.nkv, sp.S);
+      lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES, sp.S, attn_prefix_tc<HD>,
+                          tmK, tmV, a));
+    } else {
+      const Splits sp = fixed_splits(a.P);
+      dim3 grid((a.Bp * a.L * G + kQT - 1) / kQT, a.R * a.nkv, sp.S);
+      lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD>(), sp.S, attn_prefix_mma<HD>, tmK,
+                          tmV, a));
+    }
     lc.after(SF_K_ATTN_PREFIX);
   }
   dim3 grid((a.L * G + kBQT - 1) / kBQT, a.R * a.Bp * a.nkv);

@@ -113,6 +113,11 @@ BF16_CASES = {
     "no_prefix": dict(prefix_len=0, n_drafts=3),
     "three_requests_gqa7": dict(n_requests=3, n_q_heads=7, n_kv_heads=1, prefix_len=200, n_drafts=4),
     "long_prefix": dict(prefix_len=1000, n_drafts=2, block_len=64),
+    # prefixes of 2048+ keys take the tcgen05 prefix kernel (4 splits, ragged
+    # last block, several 128-vector query tiles per KV head at delta = 0)
+    "tc_prefix_hd64_ragged": dict(head_dim=64, n_q_heads=8, n_kv_heads=2, block_len=20, prefix_len=2100,
+                                  n_drafts=5),
+    "tc_prefix_three_requests_gqa7": dict(n_requests=3, n_q_heads=7, n_kv_heads=1, prefix_len=2048, n_drafts=4),
 }
 
 
