@@ -440,8 +440,8 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
 // of one request and KV head = the 128 TMEM lanes, one split of the prefix).
 // Per block of 64 keys:
 //   S = Q K^T       tcgen05.mma, Q and K K-major in shared memory, S in TMEM
-//                   (two buffers, so the next block's scores overlap this
-//                   block's softmax);
+//                   (three buffers: the scores two blocks ahead are computed
+//                   while this block's softmax runs);
 //   P = exp2(S - m) by the softmax warps, one query row per thread, written as
 //                   bf16 to shared memory (K-major, 128-byte swizzle);
 //   O += P V        tcgen05.mma, V MN-major as the TMA box leaves it, O in TMEM.
@@ -450,12 +450,14 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
 // exact because m is whatever reference the exponentials used.
 // Warp 0 streams K and V through two kTcStages-deep rings of TMA loads (lane 0
 // the keys, freed once their scores are computed; lane 1 the values, freed
-// once P V is done), warp 1 owns TMEM and issues the MMAs, warps 2-5 load Q and
-// run the softmax and the epilogue.
+// once P V is done), warp 1 owns TMEM and issues the MMAs, warps 2-9 load Q and
+// run the softmax and the epilogue: the two warps on the same 32 TMEM lanes
+// take half of each row's 64 scores and half of its output columns, and
+// exchange only the row's block maximum.
 // The split CTAs of a tile form a cluster and merge as the CUDA-core path does.
 constexpr int kTcQ = 128;
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per row group)
 constexpr int kTcMinKeysPerSplit = 512;
 constexpr int kTcMaxSplits = 4;
 // Prefixes of at least this many keys take the tcgen05 kernel; shorter ones
@@ -486,11 +488,20 @@ struct TcLayout {
   static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
   static constexpr int BYTES = OFF_BAR + 256 + 1024;   // + alignment of the dynamic window
   static constexpr int XLD = HD + 4;                    // merge exchange row: o[HD], m, l (16-byte rows)
-  static constexpr int TMEM_COLS = 256;                 // S0 [0,64), S1 [64,128), O [128, 128 + HD)
+  static constexpr int SBUF = 3;                        // score buffers: columns [64 s, 64 s + 64)
+  static constexpr int O_COL = 256;                     // O: columns [256, 256 + HD)
+  static constexpr int TMEM_COLS = 512;
   static_assert((kTcQ + kMaxSplits - 1) * XLD * 4 <= OFF_P, "merge exchange area");
 };
 
 __device__ __forceinline__ void tmem_ld32_raw(uint32_t taddr, float (&v)[32]) { tc::tmem_ld32(taddr, v); }
+
+// 2^x on the special-function unit (flushes subnormal results to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // 64 consecutive fp32 columns of this warp's 32 TMEM lanes, one wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -532,14 +543,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   uint64_t* vfull = bar + kTcStages;       // [kTcStages] V landed
   uint64_t* kempty = bar + 2 * kTcStages;  // [kTcStages] K consumed by S = Q K^T
   uint64_t* vempty = bar + 3 * kTcStages;  // [kTcStages] V consumed by O += P V
-  uint64_t* sfull = bar + 4 * kTcStages;   // [2] scores in TMEM
-  uint64_t* sempty = sfull + 2;            // [2] scores read
-  uint64_t* pfull = sempty + 2;            // [2] P written
+  uint64_t* sfull = bar + 4 * kTcStages;   // [SBUF] scores in TMEM
+  uint64_t* sempty = sfull + Lay::SBUF;    // [SBUF] scores read
+  uint64_t* pfull = sempty + Lay::SBUF;    // [2] P written
   uint64_t* pvdone = pfull + 2;            // [2] P V of that buffer done
   uint64_t* qready = pvdone + 2;
   uint64_t* ofull = qready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
   float* xbuf = reinterpret_cast<float*>(base);  // merge exchange, over Q and the ring once they are dead
+  __shared__ float xmax[2][2][kTcQ];             // [block parity][half][row]: partial block maxima
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
@@ -563,13 +575,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       tc::mbar_init(&kempty[i], 1);
       tc::mbar_init(&vempty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < Lay::SBUF; ++i) {
       tc::mbar_init(&sfull[i], 1);
-      tc::mbar_init(&sempty[i], 128);
-      tc::mbar_init(&pfull[i], 128);
+      tc::mbar_init(&sempty[i], 256);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&pfull[i], 256);
       tc::mbar_init(&pvdone[i], 1);
     }
-    tc::mbar_init(qready, 128);
+    tc::mbar_init(qready, 256);
     tc::mbar_init(ofull, 1);
     tc::fence_barrier_init();
   }
@@ -612,130 +626,154 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       const uint32_t idesc_s = tc::idesc_bf16_f32(kTcQ, kKB);
       const uint32_t idesc_pv = tc::idesc_bf16_f32(kTcQ, HD) | (1u << 16);  // V is MN-major
       tc::mbar_wait(qready, 0, a.err);
-      for (int b = 0; b <= nblk; ++b) {
-        if (b < nblk) {  // S(b) = Q K(b)^T into TMEM buffer b % 2
-          const int st = b % kTcStages, sb = b & 1;
-          tc::mbar_wait(&kfull[st], (b / kTcStages) & 1, a.err);
-          if (b >= 2) tc::mbar_wait(&sempty[sb], ((b >> 1) - 1) & 1, a.err);
-          tc::fence_after_sync();
-          const unsigned char* sk = sK + st * Lay::STAGE;
+      auto issue_s = [&](int b) {  // S(b) = Q K(b)^T into score buffer b % SBUF
+        const int st = b % kTcStages, sb = b % Lay::SBUF;
+        tc::mbar_wait(&kfull[st], (b / kTcStages) & 1, a.err);
+        if (b >= Lay::SBUF) tc::mbar_wait(&sempty[sb], ((b / Lay::SBUF) - 1) & 1, a.err);
+        tc::fence_after_sync();
+        const unsigned char* sk = sK + st * Lay::STAGE;
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint64_t dq = tc::sw128_kmajor_desc(smem_addr(sQ + (kk >> 2) * Lay::HALF + (kk & 3) * 32));
-            const uint64_t dk = tc::sw128_kmajor_desc(smem_addr(sk + (kk >> 2) * Lay::KV_TILE + (kk & 3) * 32));
-            tc::mma_bf16(tmem + sb * kKB, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(&sfull[sb]);
-          tc::mma_commit(&kempty[st]);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t dq = tc::sw128_kmajor_desc(smem_addr(sQ + (kk >> 2) * Lay::HALF + (kk & 3) * 32));
+          const uint64_t dk = tc::sw128_kmajor_desc(smem_addr(sk + (kk >> 2) * Lay::KV_TILE + (kk & 3) * 32));
+          tc::mma_bf16(tmem + sb * kKB, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
         }
-        if (b >= 1) {  // O += P(j) V(j), j = b - 1
-          const int j = b - 1, st = j % kTcStages, pb = j & 1;
-          tc::mbar_wait(&pfull[pb], (j >> 1) & 1, a.err);
-          tc::mbar_wait(&vfull[st], (j / kTcStages) & 1, a.err);
-          tc::fence_after_sync();
-          const unsigned char* sv = sV + st * Lay::STAGE;
+        tc::mma_commit(&sfull[sb]);
+        tc::mma_commit(&kempty[st]);
+      };
+      for (int b = 0; b < min(Lay::SBUF - 1, nblk); ++b) issue_s(b);
+      for (int j = 0; j < nblk; ++j) {
+        // the scores SBUF - 1 blocks ahead, as soon as their buffer is read
+        if (j + Lay::SBUF - 1 < nblk) issue_s(j + Lay::SBUF - 1);
+        // O += P(j) V(j)
+        const int st = j % kTcStages, pb = j & 1;
+        tc::mbar_wait(&pfull[pb], (j >> 1) & 1, a.err);
+        tc::mbar_wait(&vfull[st], (j / kTcStages) & 1, a.err);
+        tc::fence_after_sync();
+        const unsigned char* sv = sV + st * Lay::STAGE;
 #pragma unroll
-          for (int kk = 0; kk < kKB / 16; ++kk) {
-            const uint64_t dp = tc::sw128_kmajor_desc(smem_addr(sP + pb * Lay::P_TILE + kk * 32));
-            const uint64_t dv = tc::sw128_mnmajor_desc(smem_addr(sv + kk * 2048), Lay::KV_TILE);
-            tc::mma_bf16(tmem + 2 * kKB, dp, dv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc::mma_commit(&pvdone[pb]);
-          tc::mma_commit(&vempty[st]);
+        for (int kk = 0; kk < kKB / 16; ++kk) {
+          const uint64_t dp = tc::sw128_kmajor_desc(smem_addr(sP + pb * Lay::P_TILE + kk * 32));
+          const uint64_t dv = tc::sw128_mnmajor_desc(smem_addr(sv + kk * 2048), Lay::KV_TILE);
+          tc::mma_bf16(tmem + Lay::O_COL, dp, dv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
+        tc::mma_commit(&pvdone[pb]);
+        tc::mma_commit(&vempty[st]);
       }
       tc::mma_commit(ofull);
     }
     __syncwarp();
   } else {
-    // softmax warps: TMEM lanes 32 * (warp % 4) .. + 31, one query row per thread
-    const int row = 32 * (warp & 3) + lane;
-    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    // softmax warps: TMEM lanes 32 * (warp % 4) .. + 31, one query row per
+    // thread pair; `half` selects 32 of the row's 64 scores and HD / 2 of its
+    // output columns
+    const int grp = warp & 3, half = (warp - 2) >> 2;
+    const int row = 32 * grp + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * grp) << 16);
     const int v = q0 + row;
     {
       const bool ok = v < nqv;
       const int g = off_r + (ok ? v / G : 0), h = kvh * G + (ok ? v % G : 0);
       const bf16* src = qkv + (size_t)g * a.ld_qkv + h * HD;
 #pragma unroll
-      for (int c = 0; c < HD / 8; ++c)
+      for (int c = half * (HD / 16); c < (half + 1) * (HD / 16); ++c)
         cp_async16(sQ + (c >> 3) * Lay::HALF + row * 128 + (((c & 7) ^ (row & 7)) << 4), src + c * 8, ok);
       cp_async_commit();
       cp_async_wait<0>();
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(qready);
     }
+    const float scale = a.scale_log2;
+    // running max in raw score units, partial denominator of this thread's keys
     float m_ref = -INFINITY, l = 0.f;
     for (int b = 0; b < nblk; ++b) {
-      const int sb = b & 1;
-      tc::mbar_wait(&sfull[sb], (b >> 1) & 1, a.err);
+      const int sb = b % Lay::SBUF, pbuf = b & 1;
+      tc::mbar_wait(&sfull[sb], (b / Lay::SBUF) & 1, a.err);
       tc::fence_after_sync();
-      float sc[kKB];
-      tmem_ld64(tl + sb * kKB, sc);
+      float sc[32];
+      tmem_ld32_raw(tl + sb * kKB + 32 * half, sc);
       tc::fence_before_sync();
       tc::mbar_arrive(&sempty[sb]);
-      const int kb0 = k_lo + b * kKB;
-      float mb = -INFINITY;
+      const int kb0 = k_lo + b * kKB + 32 * half;
+      if (kb0 + 32 > k_hi) {  // the split's last block may be ragged
 #pragma unroll
-      for (int k = 0; k < kKB; ++k) {
-        sc[k] = kb0 + k < k_hi ? sc[k] * a.scale_log2 : -INFINITY;
-        mb = fmaxf(mb, sc[k]);
+        for (int k = 0; k < 32; ++k)
+          if (kb0 + k >= k_hi) sc[k] = -INFINITY;
       }
+      float mx = sc[0];
+#pragma unroll
+      for (int k = 1; k < 32; ++k) mx = fmaxf(mx, sc[k]);
+      // the row's block maximum: exchange with the partner warp (double-buffered by block parity)
+      xmax[pbuf][half][row] = mx;
+      tc::named_bar_sync(1 + grp, 64);
+      const float mb = fmaxf(mx, xmax[pbuf][half ^ 1][row]);
       if (b == 0) {
         m_ref = mb;
       } else {
-        const bool need = mb > m_ref + kTcRescaleLog2;
+        const bool need = (mb - m_ref) * scale > kTcRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {  // warp-wide: the TMEM accesses are collective
           const float m_new = need ? mb : m_ref;
-          const float f = exp2f(m_ref - m_new);
+          const float f = ex2_approx((m_ref - m_new) * scale);
           // O holds every block before b once P V of block b - 1 is done
           tc::mbar_wait(&pvdone[(b - 1) & 1], ((b - 1) >> 1) & 1, a.err);
           tc::fence_after_sync();
 #pragma unroll
-          for (int c0 = 0; c0 < HD; c0 += 32) {
+          for (int c0 = half * (HD / 2); c0 < (half + 1) * (HD / 2); c0 += 32) {
             float o[32];
-            tmem_ld32_raw(tl + 2 * kKB + c0, o);
+            tmem_ld32_raw(tl + Lay::O_COL + c0, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= f;
-            tc::tmem_st32(tl + 2 * kKB + c0, o);
+            for (int i2 = 0; i2 < 32; ++i2) o[i2] *= f;
+            tc::tmem_st32(tl + Lay::O_COL + c0, o);
           }
           tc::tmem_wait_st();
           l *= f;
           m_ref = m_new;
         }
       }
+      const float mneg = -m_ref * scale;
       float ls = 0.f;
-      uint32_t pk[kKB / 2];
+      uint32_t pk[16];
 #pragma unroll
-      for (int k = 0; k < kKB; k += 2) {
-        const float p0 = exp2f(sc[k] - m_ref), p1 = exp2f(sc[k + 1] - m_ref);
+      for (int k = 0; k < 32; k += 2) {
+        const float p0 = ex2_approx(fmaf(sc[k], scale, mneg)), p1 = ex2_approx(fmaf(sc[k + 1], scale, mneg));
         ls += p0 + p1;
         pk[k / 2] = pack_bf16(p0, p1);
       }
       l += ls;
-      // P buffer sb is free once P V of block b - 2 is done
-      if (b >= 2) tc::mbar_wait(&pvdone[sb], ((b - 2) >> 1) & 1, a.err);
-      unsigned char* prow = sP + sb * Lay::P_TILE + row * 128;
+      // P buffer b % 2 is free once P V of block b - 2 is done
+      if (b >= 2) tc::mbar_wait(&pvdone[pbuf], ((b - 2) >> 1) & 1, a.err);
+      unsigned char* prow = sP + pbuf * Lay::P_TILE + row * 128;
 #pragma unroll
-      for (int c = 0; c < kKB / 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(prow + (((4 * half + c) ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      tc::mbar_arrive(&pfull[sb]);
+      tc::mbar_arrive(&pfull[pbuf]);
     }
+    // the row's denominator: both halves (through the buffer of the next
+    // block parity, which the partner no longer reads)
+    xmax[nblk & 1][half][row] = l;
+    tc::named_bar_sync(1 + grp, 64);
+    const float lrow = l + xmax[nblk & 1][half ^ 1][row];
+    const float mrow = m_ref * scale;
     tc::mbar_wait(ofull, 0, a.err);
     tc::fence_after_sync();
-    float o[HD];
+    constexpr int HO = HD / 2;
+    float o[HO];
 #pragma unroll
-    for (int c0 = 0; c0 < HD; c0 += 32) tmem_ld32_raw(tl + 2 * kKB + c0, *reinterpret_cast<float(*)[32]>(o + c0));
+    for (int c0 = 0; c0 < HO; c0 += 32)
+      tmem_ld32_raw(tl + Lay::O_COL + half * HO + c0, *reinterpret_cast<float(*)[32]>(o + c0));
     if (sp.S == 1) {  // a single split: the partial is already the merged state
       if (v < nqv) {
         const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
-        float* po = a.part_o + qi * HD;
+        float* po = a.part_o + qi * HD + half * HO;
 #pragma unroll
-        for (int c = 0; c < HD; c += 4) *reinterpret_cast<float4*>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        a.part_ml[qi * 2 + 0] = m_ref;
-        a.part_ml[qi * 2 + 1] = l;
+        for (int c = 0; c < HO; c += 4) *reinterpret_cast<float4*>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        if (half == 0) {
+          a.part_ml[qi * 2 + 0] = mrow;
+          a.part_ml[qi * 2 + 1] = lrow;
+        }
       }
     } else {
       // rows [rank * per, (rank + 1) * per) of the tile are merged by `rank`
@@ -746,18 +784,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       const uint32_t dst =
           tc::map_to_rank(smem_addr(xbuf + ((size_t)s * per + (row - owner * per)) * Lay::XLD), (uint32_t)owner);
 #pragma unroll
-      for (int c = 0; c < HD; c += 4)
-        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + c * 4), "f"(o[c]), "f"(o[c + 1]),
-                     "f"(o[c + 2]), "f"(o[c + 3])
+      for (int c = 0; c < HO; c += 4)
+        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (half * HO + c) * 4), "f"(o[c]),
+                     "f"(o[c + 1]), "f"(o[c + 2]), "f"(o[c + 3])
                      : "memory");
-      asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(dst + HD * 4), "f"(m_ref), "f"(l) : "memory");
+      if (half == 0)
+        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(dst + HD * 4), "f"(mrow), "f"(lrow) : "memory");
     }
   }
   if (sp.S > 1) {
     if (warp < 2)  // the producer and MMA warps take part in the cluster barriers too
       asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    // merge: one warp per row (warps 0-5), split weights formed once per row
+    // merge: one warp per row (all warps), split weights formed once per row
     const int rows = min((kTcQ + sp.S - 1) / sp.S, kTcQ - s * ((kTcQ + sp.S - 1) / sp.S));
     const int per = (kTcQ + sp.S - 1) / sp.S;
     for (int rl = warp; rl < rows; rl += kTcThreads / 32) {
