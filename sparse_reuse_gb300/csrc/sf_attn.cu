@@ -259,7 +259,10 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   uint64_t* full = reinterpret_cast<uint64_t*>(base + kStages * STAGE + kQT * LD * 2);
   float* xbuf = reinterpret_cast<float*>(base);  // exchange area, reused after the loop
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
+  // grid: x = (request, KV head), y = query tile, z = split; the first query
+  // tiles of every (request, KV head) are dispatched first, and the tiles that
+  // only a larger recompute set would fill come last
+  const int r = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
   const Splits sp = fixed_splits(a.P);
   const int G = a.nq / a.nkv;
   // Every kernel of the pass lets its dependants start only after its own
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   // when this grid starts: the recompute offsets (gate kernel) can be read
   // before the wait, past L1.  Only the queries (previous kernel) wait.
   const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
-  const int q0 = blockIdx.x * kQT;
+  const int q0 = blockIdx.y * kQT;
   if (q0 >= nqv) {  // uniform over the cluster
     pdl_wait();
     return;
@@ -554,12 +557,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   __shared__ float xmax[2][2][kTcQ];             // [block parity][half][row]: partial block maxima
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
+  // grid: x = (request, KV head), y = query tile, z = split; the first query
+  // tiles of every (request, KV head) are dispatched first, and the tiles that
+  // only a larger recompute set would fill come last
+  const int r = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
   const Splits sp = tc_splits(a.P);
   const int G = a.nq / a.nkv;
   // recompute offsets from the gate kernel (complete once this grid runs), past L1
   const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
-  const int q0 = blockIdx.x * kTcQ;
+  const int q0 = blockIdx.y * kTcQ;
   if (q0 >= nqv) {  // uniform over the cluster
     pdl_wait();
     return;
@@ -1133,12 +1139,12 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
     lc.before(SF_K_ATTN_PREFIX);
     if (a.P >= kTcMinPrefix) {
       const Splits sp = tc_splits(a.P);
-      dim3 grid((a.Bp * a.L * G + kTcQ - 1) / kTcQ, a.R * a.nkv, sp.S);
+      dim3 grid(a.R * a.nkv, (a.Bp * a.L * G + kTcQ - 1) / kTcQ, sp.S);
       lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES, sp.S, attn_prefix_tc<HD>,
                           tmK, tmV, a));
     } else {
       const Splits sp = fixed_splits(a.P);
-      dim3 grid((a.Bp * a.L * G + kQT - 1) / kQT, a.R * a.nkv, sp.S);
+      dim3 grid(a.R * a.nkv, (a.Bp * a.L * G + kQT - 1) / kQT, sp.S);
       lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD>(), sp.S, attn_prefix_mma<HD>, tmK,
                           tmV, a));
     }
