@@ -130,8 +130,20 @@ sf_status sf_verify(sf_ctx* ctx, void* stream, const void* hidden_in, const int3
 sf_status sf_set_debug(sf_ctx* ctx, float* layer_hidden, int32_t* rc_rows);
 
 /* Wait for the context's work on `stream` to finish and report a device-side
- * check that fired (SF_ERR_DEVICE_ASSERT) or a CUDA error. */
+ * check that fired (SF_ERR_DEVICE_ASSERT) or a CUDA error.  A device-side
+ * check word is reported once: it is cleared on return, so a caller that
+ * handled the failure can go on using the context (a bounded wait that ran out
+ * leaves no GPU fault behind, only wrong values in that pass). */
 sf_status sf_sync_status(sf_ctx* ctx, void* stream);
+
+/* Failure injection for tests of the detection path (no counterpart in the
+ * method): while `on` is nonzero, later sf_verify passes never signal the
+ * completion of layer 0's compaction.  The recompute rows' bounded waits for
+ * it give up after about 2 s and raise the timeout bit of the device check
+ * word; the pass finishes with wrong values and sf_sync_status reports
+ * SF_ERR_DEVICE_ASSERT.  No GPU fault, trap or hang is involved.
+ * Errors: SF_ERR_INVALID_ARG (null ctx). */
+sf_status sf_inject_stall(sf_ctx* ctx, int on);
 
 /* Free everything the context owns (synchronises the device first). */
 sf_status sf_destroy(sf_ctx* ctx);

@@ -28,7 +28,7 @@ SF_K_COUNT = len(FAMILIES)
 # every symbol include/specfold.h declares
 EXPORTS = ["sf_create", "sf_verify", "sf_set_debug", "sf_sync_status", "sf_destroy", "sf_status_str",
            "sf_last_error", "sf_get_stats", "sf_set_graphs", "sf_timing_begin", "sf_timing_read",
-           "sfk_gemm_bf16", "sfk_gate_noalloc"]
+           "sfk_gemm_bf16", "sfk_gate_noalloc", "sf_inject_stall"]
 
 
 class SfShapes(ctypes.Structure):
@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
     lib.sf_verify.argtypes = [vp, vp, vp, i32p, vp, vp, c_int, c_int, c_int, c_float, vp, vp, vp, vp]
     lib.sf_set_debug.argtypes = [vp, vp, vp]
     lib.sf_sync_status.argtypes = [vp, vp]
+    lib.sf_inject_stall.argtypes = [vp, c_int]
     lib.sf_destroy.argtypes = [vp]
     lib.sf_status_str.argtypes = [c_int]
     lib.sf_status_str.restype = ctypes.c_char_p
@@ -144,6 +145,10 @@ def sf_set_debug(ctx, layer_hidden, rc_rows) -> None:
 
 def sf_sync_status(ctx, stream) -> None:
     _check(lib.sf_sync_status(ctx, stream), ctx, "sf_sync_status")
+
+
+def sf_inject_stall(ctx, on: bool) -> None:
+    _check(lib.sf_inject_stall(ctx, int(bool(on))), ctx, "sf_inject_stall")
 
 
 def sf_destroy(ctx) -> None:

@@ -180,6 +180,7 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     ga.gain = W.g1;
     ga.eps = s.rms_eps;
     ga.done = c->epoch + 1;
+    ga.stall = c->inject_stall && l == 0;
     ga.epoch = c->epoch;
     ga.layer = l;
     if (launch_gate_norm(lc, ga, bf16) != cudaSuccess) return lc.err;
@@ -404,6 +405,7 @@ sf_status sf_verify(sf_ctx* c, void* stream, const void* hidden_in, const int32_
     sf_graph_key key;
     key.hidden_in = hidden_in; key.prefix_k = prefix_k; key.prefix_v = prefix_v; key.hidden_out = hidden_out;
     key.fold = fold_mask; key.src = src; key.rc_count = rc_count; key.dbg_hidden = c->dbg_hidden;
+    key.stall = c->inject_stall;
     key.dbg_rc = c->dbg_rc; key.stream = stream; key.R = R; key.B = B; key.P = P; key.delta = delta;
     key.parent.assign(parent, parent + R * Bp);
     if (!(c->graph_valid && key == c->graph_key)) {
@@ -490,8 +492,21 @@ sf_status sf_sync_status(sf_ctx* c, void* stream) {
   unsigned w = 0;
   e = cudaMemcpy(&w, c->err_dev, sizeof(unsigned), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail(c, SF_ERR_CUDA, "reading the device check word: %s", cudaGetErrorString(e));
-  *c->err_host = w;
-  if (w) return fail(c, SF_ERR_DEVICE_ASSERT, "device check word 0x%x", w);
+  if (w) {
+    // reported once: the word is cleared so that the caller can continue
+    e = cudaMemset(c->err_dev, 0, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    *c->err_host = 0;
+    if (e != cudaSuccess) return fail(c, SF_ERR_CUDA, "clearing the device check word: %s", cudaGetErrorString(e));
+    return fail(c, SF_ERR_DEVICE_ASSERT, "device check word 0x%x", w);
+  }
+  *c->err_host = 0;
+  return SF_OK;
+}
+
+sf_status sf_inject_stall(sf_ctx* c, int on) {
+  if (!c) return SF_ERR_INVALID_ARG;
+  c->inject_stall = on ? 1 : 0;
   return SF_OK;
 }
 

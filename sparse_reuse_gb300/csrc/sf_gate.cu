@@ -341,7 +341,8 @@ __global__ void __launch_bounds__(256) gate_norm_kernel(const __grid_constant__ 
       s_slot = slot[row];
       // after compact's closing block barrier this release covers every
       // thread's writes of the list, the recompute rows' slots and the offsets
-      st_release_gpu(a.done, tag);
+      // (a failure-injection pass leaves the tag unset: the waits run out)
+      if (!a.stall) st_release_gpu(a.done, tag);
     }
     // the folded rows' sources are resolved while the recompute rows write
     resolve(a, flags, slot);

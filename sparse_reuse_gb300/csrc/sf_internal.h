@@ -35,12 +35,13 @@ struct sf_graph_key {
   void* stream = nullptr;
   int R = 0, B = 0, P = 0;
   float delta = 0.f;
+  int stall = 0;
   std::vector<int> parent;
   bool operator==(const sf_graph_key& o) const {
     return hidden_in == o.hidden_in && prefix_k == o.prefix_k && prefix_v == o.prefix_v &&
            hidden_out == o.hidden_out && fold == o.fold && src == o.src && rc_count == o.rc_count &&
            dbg_hidden == o.dbg_hidden && dbg_rc == o.dbg_rc && stream == o.stream && R == o.R &&
-           B == o.B && P == o.P && delta == o.delta && parent == o.parent;
+           B == o.B && P == o.P && delta == o.delta && stall == o.stall && parent == o.parent;
   }
 };
 
@@ -79,6 +80,7 @@ struct sf_ctx {
 
   float* dbg_hidden = nullptr;
   int32_t* dbg_rc = nullptr;
+  int inject_stall = 0;  // failure injection: layer 0's compaction never signals completion
 
   sf_stats stats{};
   bool use_graphs = true;
@@ -165,6 +167,7 @@ struct GateArgs {
   const float* gain;      // [d] attention RMSNorm gain
   float eps;
   unsigned* done;         // completion tag of the layer's compaction
+  int stall;              // failure injection: the tag is never set, so its waits run out
   const unsigned* epoch;  // pass counter, advanced by the final residual kernel
   int layer;
 };
