@@ -136,18 +136,18 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Scores of this warp's 16 query rows against 64 keys in smem (rows = keys).
-template <int HD>
-__device__ __forceinline__ void qk_scores(float (&sc)[kKB / 8][4], const uint32_t (&qf)[HD / 16][4], const bf16* K,
+// Scores of this warp's 16 query rows against KB keys in smem (rows = keys).
+template <int HD, int KB>
+__device__ __forceinline__ void qk_scores(float (&sc)[KB / 8][4], const uint32_t (&qf)[HD / 16][4], const bf16* K,
                                           int lane) {
   constexpr int LD = HD + 8;
 #pragma unroll
-  for (int nt = 0; nt < kKB / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  for (int nt = 0; nt < KB / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
   const int j = lane >> 3;
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
-    for (int n2 = 0; n2 < kKB / 16; ++n2) {
+    for (int n2 = 0; n2 < KB / 16; ++n2) {
       uint32_t kf[4];
       ldsm_x4(kf, K + (n2 * 16 + (j >> 1) * 8 + (lane & 7)) * LD + kk * 16 + (j & 1) * 8);
       mma16816(sc[2 * n2], qf[kk], kf[0], kf[1]);
@@ -157,13 +157,13 @@ __device__ __forceinline__ void qk_scores(float (&sc)[kKB / 8][4], const uint32_
 }
 
 // o += P V for this warp's 16 rows; P in the score accumulators (bf16-rounded).
-template <int HD>
-__device__ __forceinline__ void pv_accum(float (&o)[HD / 8][4], const float (&p)[kKB / 8][4], const bf16* V,
+template <int HD, int KB>
+__device__ __forceinline__ void pv_accum(float (&o)[HD / 8][4], const float (&p)[KB / 8][4], const bf16* V,
                                          int lane) {
   constexpr int LD = HD + 8;
   const int j = lane >> 3;
 #pragma unroll
-  for (int kt = 0; kt < kKB / 16; ++kt) {
+  for (int kt = 0; kt < KB / 16; ++kt) {
     uint32_t pa[4] = {pack_bf16(p[2 * kt][0], p[2 * kt][1]), pack_bf16(p[2 * kt][2], p[2 * kt][3]),
                       pack_bf16(p[2 * kt + 1][0], p[2 * kt + 1][1]), pack_bf16(p[2 * kt + 1][2], p[2 * kt + 1][3])};
 #pragma unroll
@@ -851,14 +851,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
 // block keys/values are the branch's own table K_i[m] = QKV[rcslot(i, m)].
 constexpr int kBQT = 32;
 
-template <int HD>
+template <int HD, int KB>
 __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   constexpr int LD = HD + 8;
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int slot[kKB];
+  __shared__ int slot[KB];
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   bf16* sK = sQ + kBQT * LD;
-  bf16* sV = sK + kKB * LD;
+  bf16* sV = sK + KB * LD;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rb = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;  // rb = r * Bp + i
   const int G = a.nq / a.nkv, L = a.L;
@@ -875,7 +875,7 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   const int count = __ldcg(a.meta);
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
   const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
-  for (int m = tid; m < kKB; m += 64) {
+  for (int m = tid; m < KB; m += 64) {
     int g = m < L ? __ldcg(a.rcslot + rb * L + m) : 0;
     if (g < 0 || g >= count) {
       raise_error(a.err, kErrAttn);
@@ -891,7 +891,7 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
       cp_async16(sQ + row * LD + c8 * 8,
                  qkv + (size_t)slot[ok ? v / G : 0] * a.ld_qkv + (kvh * G + (ok ? v % G : 0)) * HD + c8 * 8, ok);
     }
-    for (int idx = tid; idx < kKB * (HD / 8); idx += 64) {
+    for (int idx = tid; idx < KB * (HD / 8); idx += 64) {
       const int m = idx / (HD / 8), c8 = idx % (HD / 8);
       const bf16* src = qkv + (size_t)slot[m] * a.ld_qkv;
       cp_async16(sK + m * LD + c8 * 8, src + koff + c8 * 8, m < L);
@@ -924,11 +924,11 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   __syncthreads();
   uint32_t qf[HD / 16][4];
   load_q_frags<HD>(qf, sQ, warp, lane);
-  float sc[kKB / 8][4];
-  qk_scores<HD>(sc, qf, sK, lane);
+  float sc[KB / 8][4];
+  qk_scores<HD, KB>(sc, qf, sK, lane);
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-  for (int nt = 0; nt < kKB / 8; ++nt) {
+  for (int nt = 0; nt < KB / 8; ++nt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int m = nt * 8 + (lane & 3) * 2 + (e & 1);
@@ -940,7 +940,7 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   const float mb0 = quad_max(mx0), mb1 = quad_max(mx1);
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < kKB / 8; ++nt) {
+  for (int nt = 0; nt < KB / 8; ++nt) {
     sc[nt][0] = exp2f(sc[nt][0] - mb0);
     sc[nt][1] = exp2f(sc[nt][1] - mb0);
     sc[nt][2] = exp2f(sc[nt][2] - mb1);
@@ -952,7 +952,7 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   float o[HD / 8][4];
 #pragma unroll
   for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  pv_accum<HD>(o, sc, sV, lane);
+  pv_accum<HD, KB>(o, sc, sV, lane);
 
   bf16* out = reinterpret_cast<bf16*>(a.attn);
 #pragma unroll
@@ -1117,7 +1117,9 @@ template <int HD>
 cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   constexpr int LD = HD + 8;
   const int G = a.nq / a.nkv;
-  const size_t smem_b = (size_t)(kBQT + 2 * kKB) * LD * sizeof(bf16);
+  // block keys per CTA tile: 32 when the block length allows, else 64
+  const int kb = a.L <= 32 ? 32 : kKB;
+  const size_t smem_b = (size_t)(kBQT + 2 * kb) * LD * sizeof(bf16);
   static cudaError_t attr = [&] {
     cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcLayout<HD>::BYTES);
@@ -1125,8 +1127,11 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
       e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                prefix_smem_bytes<HD>());
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_block_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(attn_block_mma<HD, kKB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_block_mma<HD, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)((kBQT + 2 * 32) * LD * sizeof(bf16)));
     return e;
   }();
   if (attr != cudaSuccess) return lc.err = attr;
@@ -1152,7 +1157,10 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
   }
   dim3 grid((a.L * G + kBQT - 1) / kBQT, a.R * a.Bp * a.nkv);
   lc.before(SF_K_ATTN_BLOCK);
-  lc.check(launch_pdl(lc.st, grid, dim3(64), smem_b, 1, attn_block_mma<HD>, a));
+  if (kb == 32)
+    lc.check(launch_pdl(lc.st, grid, dim3(64), smem_b, 1, attn_block_mma<HD, 32>, a));
+  else
+    lc.check(launch_pdl(lc.st, grid, dim3(64), smem_b, 1, attn_block_mma<HD, kKB>, a));
   lc.after(SF_K_ATTN_BLOCK);
   return lc.err;
 }
