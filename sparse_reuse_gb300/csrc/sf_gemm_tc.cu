@@ -39,22 +39,25 @@ constexpr int THREADS = 192;
 // The pipeline's shared memory holds a ring of weight (A) tiles growing up from
 // its start and a ring of row (B) tiles growing down from its end; the number
 // of stages follows from the live row count, so a small recompute set keeps
-// up to MAX_STAGES weight tiles in flight and a full 256-row tile still has
-// MIN_STAGES.  Weight tiles fetched before the row count is known go to the
-// first MIN_STAGES slots of the A ring, which every stage count keeps.
+// up to MAX_STAGES weight tiles in flight.  Its size is a launch parameter:
+// PIPE_BYTES gives one CTA per SM, PIPE_BYTES_PAIR two (for GEMMs with more
+// tiles than SMs, which then run in one wave).  Weight tiles fetched before
+// the row count is known go to the first slots of the A ring that even a full
+// 256-row tile keeps.
 constexpr int MAX_STAGES = 12;
-constexpr int MIN_STAGES = 4;
 constexpr int PIPE_BYTES = 216 * 1024;
+constexpr int PIPE_BYTES_PAIR = 110 * 1024;
 constexpr int SMEM_BYTES = PIPE_BYTES + 1024 + 256;
-static_assert(MIN_STAGES * (A_BYTES + (BN / RC) * B_CHUNK) <= PIPE_BYTES, "a full row tile needs MIN_STAGES");
 static_assert(2 * MAX_STAGES * 8 + 8 + 4 <= 256, "barrier area");
 
-__host__ __device__ constexpr int stages_for(int n_chunks) {
-  return n_chunks <= 0 ? MIN_STAGES
-                       : (PIPE_BYTES / (A_BYTES + n_chunks * B_CHUNK) < MAX_STAGES
-                              ? PIPE_BYTES / (A_BYTES + n_chunks * B_CHUNK)
-                              : MAX_STAGES);
+// Stages of a pipeline of `pipe` bytes for row tiles of n_chunks 64-row boxes
+// (n_chunks <= 0: a full tile, the fewest stages).
+__host__ __device__ constexpr int stages_for(int pipe, int n_chunks) {
+  return pipe / (A_BYTES + (n_chunks > 0 ? n_chunks : BN / RC) * B_CHUNK) < MAX_STAGES
+             ? pipe / (A_BYTES + (n_chunks > 0 ? n_chunks : BN / RC) * B_CHUNK)
+             : MAX_STAGES;
 }
+static_assert(stages_for(PIPE_BYTES, 0) >= 4 && stages_for(PIPE_BYTES_PAIR, 0) >= 2, "a full row tile's stages");
 constexpr int STAGE_LD = 129;            // epilogue staging row stride (floats)
 
 // Split counts whose exchange buffers fit the pipeline's shared memory for a
@@ -69,16 +72,18 @@ struct Params {
   int dense_count;
   int splits;  // cluster size along z (1 = no split)
   unsigned* err;
+  int pipe;    // pipeline bytes (PIPE_BYTES or PIPE_BYTES_PAIR)
 };
 
 template <class Epi>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p, const typename Epi::Params ep) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PIPE_BYTES);
+  const int pipe = p.pipe;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pipe);
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* tfull = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   // weight tiles of the first stages do not depend on earlier kernels: start
   // streaming them before waiting for the kernel that produced the rows
-  const int npre = lead ? min(MIN_STAGES, kb1 - kb0) : 0;
+  const int npre = lead ? min(stages_for(pipe, 0), kb1 - kb0) : 0;
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < npre; ++it) {
       mbar_expect_tx_only(&full[it], A_BYTES);
@@ -134,9 +139,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_rows = active ? min(BN, count - row0) : 0;
   const int n_mma = (n_rows + 15) & ~15;
   const int n_chunks = (n_rows + RC - 1) / RC;
-  const int nst = stages_for(n_chunks);  // uniform over the cluster
+  const int nst = stages_for(pipe, n_chunks);  // uniform over the cluster
   auto sA = [&](int st) { return smem + st * A_BYTES; };
-  auto sB = [&](int st) { return smem + PIPE_BYTES - (st + 1) * n_chunks * B_CHUNK; };
+  auto sB = [&](int st) { return smem + pipe - (st + 1) * n_chunks * B_CHUNK; };
   const int q = warp & 3;
   const int f = q * 32 + lane;
   const int ew = warp - 2;
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // partials of every rank for it at buf[rank][j / S][feature]
     const int n_slot = (n_rows + S - 1) / S;
     float* buf = reinterpret_cast<float*>(smem);
-    const bool fits = (size_t)S * n_slot * BM * 4 <= (size_t)PIPE_BYTES;  // S * ceil(256 / S) rows always fit
+    const bool fits = (size_t)S * n_slot * BM * 4 <= (size_t)pipe;  // S * ceil(256 / S) rows fit PIPE_BYTES
     if (threadIdx.x == 0 && !fits) raise_error(p.err, kErrGemm);
     fence_before_sync();
     cluster_sync_all();  // every CTA of the tile is past its main loop
@@ -395,9 +400,12 @@ template <class Epi>
 cudaError_t launch_tc(const TcGemm& g, const typename Epi::Params& ep, cudaStream_t st) {
   cudaError_t e = set_smem_attr<Epi>();
   if (e != cudaSuccess) return e;
-  tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err};
+  // a single-split GEMM with more tiles than SMs runs two CTAs per SM, all in one wave
+  const int m_tiles_live = (g.M / tc::BM) * (g.count ? 1 : (g.dense_count + tc::BN - 1) / tc::BN);
+  const int pipe = g.splits == 1 && m_tiles_live > sm_count() ? tc::PIPE_BYTES_PAIR : tc::PIPE_BYTES;
+  tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err, pipe};
   return launch_pdl(st, dim3(g.M / tc::BM, (g.max_rows + tc::BN - 1) / tc::BN, g.splits), dim3(tc::THREADS),
-                    tc::SMEM_BYTES, g.splits, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p, ep);
+                    (size_t)pipe + 1024 + 256, g.splits, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p, ep);
 }
 
 }  // namespace
