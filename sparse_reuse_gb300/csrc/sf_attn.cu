@@ -271,10 +271,11 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   // before the wait, past L1.  Only the queries (previous kernel) wait.
   const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
   const int q0 = blockIdx.y * kQT;
-  if (q0 >= nqv) {  // uniform over the cluster
-    pdl_wait();
-    return;
-  }
+  // An empty tile leaves without the dependency wait: it reads nothing of the
+  // previous kernel, and the live tiles (the main branch always recomputes,
+  // so there is one per request and KV head) still hold the next kernel back
+  // until they have waited.  Uniform over the cluster.
+  if (q0 >= nqv) return;
   const int s = sp.S > 1 ? (int)cluster_rank() : 0;
   const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
   const int nblk = k_hi > k_lo ? (k_hi - k_lo + kKB - 1) / kKB : 0;
@@ -469,13 +470,23 @@ constexpr int kTcMinPrefix = 2048;
 constexpr float kTcRescaleLog2 = 8.f;
 
 // Few long splits: the fixed cost of a CTA (TMEM, barriers, the first scores,
-// the epilogue) is paid once per split.
-__host__ __device__ __forceinline__ Splits tc_splits(int P) {
-  if (P <= 0) return {0, 0};
-  int S = (P + kTcMinKeysPerSplit - 1) / kTcMinKeysPerSplit;
-  S = S < 1 ? 1 : (S > kTcMaxSplits ? kTcMaxSplits : S);
+// the epilogue) is paid once per split, so S is the smallest count that still
+// fills about one wave of SMs.  A folded pass leaves about two live query
+// tiles per (request, KV head) -- the main branch and a ragged remainder --
+// so the host aims at target / (2 R nkv) splits, never below 512 keys each.
+// The kernel reads S back from the grid, so both sides agree by construction.
+__host__ __device__ __forceinline__ Splits tc_split_len(int P, int S) {
+  if (P <= 0 || S <= 0) return {0, 0};
   const int len = (((P + S - 1) / S) + kKB - 1) / kKB * kKB;
   return {(P + len - 1) / len, len};
+}
+
+inline Splits tc_splits(int P, int groups, int target_ctas) {
+  int S = target_ctas / (2 * (groups > 0 ? groups : 1));
+  const int by_len = P / kTcMinKeysPerSplit;
+  S = S > by_len ? by_len : S;
+  S = S < 1 ? 1 : (S > kTcMaxSplits ? kTcMaxSplits : S);
+  return tc_split_len(P, S);
 }
 
 template <int HD>
@@ -561,15 +572,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   // tiles of every (request, KV head) are dispatched first, and the tiles that
   // only a larger recompute set would fill come last
   const int r = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
-  const Splits sp = tc_splits(a.P);
+  const Splits sp = tc_split_len(a.P, (int)gridDim.z);
   const int G = a.nq / a.nkv;
   // recompute offsets from the gate kernel (complete once this grid runs), past L1
   const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
   const int q0 = blockIdx.y * kTcQ;
-  if (q0 >= nqv) {  // uniform over the cluster
-    pdl_wait();
-    return;
-  }
+  // An empty tile leaves without the dependency wait: it reads nothing of the
+  // previous kernel, and the live tiles (the main branch always recomputes,
+  // so there is one per request and KV head) still hold the next kernel back
+  // until they have waited.  Uniform over the cluster.
+  if (q0 >= nqv) return;
   const int s = sp.S > 1 ? (int)tc::cluster_ctarank() : 0;
   const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
   const int nblk = (k_hi - k_lo + kKB - 1) / kKB;
@@ -1143,7 +1155,7 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
     // worst case: every row of a request recomputes
     lc.before(SF_K_ATTN_PREFIX);
     if (a.P >= kTcMinPrefix) {
-      const Splits sp = tc_splits(a.P);
+      const Splits sp = tc_splits(a.P, a.R * a.nkv, a.target_ctas);
       dim3 grid(a.R * a.nkv, (a.Bp * a.L * G + kTcQ - 1) / kTcQ, sp.S);
       lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES, sp.S, attn_prefix_tc<HD>,
                           tmK, tmV, a));
