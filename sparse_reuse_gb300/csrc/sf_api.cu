@@ -140,6 +140,7 @@ cudaError_t run_gemm(sf_ctx* c, Launch& lc, int fam, const GemmArgs& g, const CU
   const int n_tiles = g.count ? 1 : (g.dense_count + 255) / 256;
   t.splits = gemm_tc_splits(g.M, g.K, n_tiles);
   t.err = c->err_dev;
+  t.count_early = g.count && g.count_early;
   return launch_gemm_tc(lc, fam, t, kind, e);
 }
 
@@ -219,6 +220,7 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     e = EpiArgs{};
     g.X = c->xn; g.ldx = d; g.W = W.wgu; g.ldw = d; g.M = c->Mgu; g.K = d;
     g.count = c->meta; g.dense_count = T; g.max_rows = T;
+    g.count_early = true;  // from the gate kernel, before the projection
     e.u = c->u; e.u_ld = c->Fp;
     if (run_gemm(c, lc, SF_K_GEMM_GATEUP, g, &W.tm_wgu, &c->tm_xn, kEpiSwiGLU, e) != cudaSuccess) return lc.err;
 
@@ -226,6 +228,7 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     e = EpiArgs{};
     g.X = c->u; g.ldx = c->Fp; g.W = W.wd; g.ldw = c->Fp; g.M = d; g.K = c->Fp;
     g.count = c->meta; g.dense_count = T; g.max_rows = T;
+    g.count_early = true;
     e.y = c->fphys; e.y_ld = d;
     if (run_gemm(c, lc, SF_K_GEMM_DOWN, g, &W.tm_wd, &c->tm_u, kEpiStore, e) != cudaSuccess) return lc.err;
   }

@@ -6,7 +6,9 @@
 //
 // prefetch() issues the row's global reads (residual input, rotary table)
 // and apply() consumes them, so a warp can start the reads of several rows
-// before it waits on any of them.
+// before it waits on any of them.  An epilogue with kStaged set copies the
+// small tables it reads into shared memory once per tile instead (stage(),
+// while the main loop runs), so its rows read only shared memory.
 #pragma once
 
 #include "sf_common.cuh"
@@ -29,15 +31,36 @@ struct EpiQKV {
     int L;
     int P;
     const float2* rope;  // [pos][hd/2] (cos, sin)
+    // bound by stage(): the rotary rows of positions P..P+L-1 and the block
+    // position n of rows row_base.. in shared memory (null: global reads)
+    const float2* s_cs = nullptr;
+    const int* s_n = nullptr;
+    int row_base = 0;
   };
   struct Pre {
     float2 cs[4];
   };
+  static constexpr bool kStaged = true;
+  // shared memory of the staged tables for a tile of up to 256 rows
+  static __host__ __device__ int stage_bytes(const Params& p) { return p.L * (p.hd >> 1) * 8 + 256 * 4; }
+  // Run by the 128 epilogue threads (t = 0..127) of a tile of n_rows rows
+  // from row0; the rows sit at P + n with n < L, so L rotary rows cover all.
+  static __device__ __forceinline__ void stage(Params& p, unsigned char* sm, int row0, int n_rows, int t) {
+    const int nf4 = p.L * (p.hd >> 1) / 2;  // float2 pairs as float4
+    float4* cs = reinterpret_cast<float4*>(sm);
+    int* sn = reinterpret_cast<int*>(sm + (size_t)nf4 * 16);
+    const float4* src = reinterpret_cast<const float4*>(p.rope + (size_t)p.P * (p.hd >> 1));
+    for (int i = t; i < nf4; i += 128) cs[i] = src[i];
+    for (int j = t; j < n_rows; j += 128) sn[j] = p.rc[row0 + j] % p.L;
+    p.s_cs = reinterpret_cast<const float2*>(cs);
+    p.s_n = sn;
+    p.row_base = row0;
+  }
   static __device__ __forceinline__ void prefetch(const Params& p, int g, int m0, int lane, Pre& pre) {
-    const int pos = p.P + (p.rc[g] % p.L);
     const int half = p.hd >> 1;
     // m0 is a multiple of 128 and hd divides 128, so j % half = (lane + 32c) % half
-    const float2* row = p.rope + (size_t)pos * half;
+    const float2* row = p.s_cs ? p.s_cs + (size_t)p.s_n[g - p.row_base] * half
+                               : p.rope + (size_t)(p.P + (p.rc[g] % p.L)) * half;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int f = m0 + lane + 32 * c;
@@ -45,11 +68,12 @@ struct EpiQKV {
     }
   }
   // hd = 128: a tile is one head, feature l + 32c pairs with l + 32(c ^ 2);
-  // hd = 64: a tile is two heads, the pair is l + 32(c ^ 1).  The partner is a
-  // compile-time index in both cases, so v stays in registers.
-  template <int PAIR>
-  static __device__ __forceinline__ void rotate_store(const Params& p, int g, int m0, int lane, const float v[4],
-                                                      const Pre& pre) {
+  // hd = 64: a tile is two heads, the pair is l + 32(c ^ 1).  Both partners
+  // are register operands and the choice is a select, so one copy of the code
+  // serves both widths.
+  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
+                                               const Pre& pre) {
+    const bool h128 = p.hd == 128;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int f = m0 + lane + 32 * c;
@@ -57,19 +81,13 @@ struct EpiQKV {
       float o = v[c];
       if (f < p.qk_dim) {
         const float2 cs = pre.cs[c];
-        const float w = v[c ^ PAIR];
+        const float w = h128 ? v[c ^ 2] : v[c ^ 1];
         // the first half of each head subtracts the partner, the second adds it
-        o = ((c & PAIR) == 0) ? (v[c] * cs.x - w * cs.y) : (v[c] * cs.x + w * cs.y);
+        const bool first = h128 ? (c & 2) == 0 : (c & 1) == 0;
+        o = first ? (v[c] * cs.x - w * cs.y) : (v[c] * cs.x + w * cs.y);
       }
       p.qkv[(size_t)g * p.ld + f] = from_f32<TAct>(o);
     }
-  }
-  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
-                                               const Pre& pre) {
-    if (p.hd == 128)
-      rotate_store<2>(p, g, m0, lane, v, pre);
-    else
-      rotate_store<1>(p, g, m0, lane, v, pre);
   }
 };
 
@@ -84,6 +102,7 @@ struct EpiResidual {
   struct Pre {
     float H[4];
   };
+  static constexpr bool kStaged = false;
   static __device__ __forceinline__ void prefetch(const Params& p, int g, int m0, int lane, Pre& pre) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) pre.H[c] = p.H[(size_t)g * p.ld + m0 + lane + 32 * c];
@@ -104,6 +123,7 @@ struct EpiSwiGLU {
     int ld;
   };
   struct Pre {};
+  static constexpr bool kStaged = false;
   static __device__ __forceinline__ void prefetch(const Params&, int, int, int, Pre&) {}
   static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
                                                const Pre&) {
@@ -124,6 +144,7 @@ struct EpiStore {
     int ld;
   };
   struct Pre {};
+  static constexpr bool kStaged = false;
   static __device__ __forceinline__ void prefetch(const Params&, int, int, int, Pre&) {}
   static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
                                                const Pre&) {
@@ -137,9 +158,20 @@ struct EpiStore {
 // of all of them (it can run before the accumulators are ready, e.g. while the
 // main loop streams the weights); epilogue_apply() consumes them, with getv(jj,
 // v) supplying the fp32 accumulators of row jj for this lane's four features.
+//
+// The epilogue runs once per CTA, so its code is fetched cold: an epilogue
+// whose per-row reads are cheap (none, or staged in shared memory) runs its
+// rows in a rolled loop and reads them just before use; only one with global
+// reads per row keeps eight unrolled rows and their reads in registers.
+template <class Epi>
+constexpr bool epilogue_rolled() {
+  return Epi::kStaged || sizeof(typename Epi::Pre) <= 1;
+}
+
 template <class Epi>
 __device__ __forceinline__ void epilogue_prefetch(const typename Epi::Params& ep, int row0, int stride, int nvalid,
                                                   int m0, int ew, int lane, typename Epi::Pre (&pre)[8]) {
+  if constexpr (epilogue_rolled<Epi>()) return;
 #pragma unroll
   for (int b = 0; b < 8; ++b) {
     const int jj = ew + 4 * b;
@@ -151,13 +183,24 @@ template <class Epi, class GetV>
 __device__ __forceinline__ void epilogue_apply(const typename Epi::Params& ep, int row0, int stride, int nvalid,
                                                int m0, int ew, int lane, const typename Epi::Pre (&pre)[8],
                                                GetV getv) {
-#pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    const int jj = ew + 4 * b;
-    if (jj < nvalid) {
+  if constexpr (epilogue_rolled<Epi>()) {
+#pragma unroll 1
+    for (int jj = ew; jj < nvalid; jj += 4) {
+      typename Epi::Pre one;
+      Epi::prefetch(ep, row0 + jj * stride, m0, lane, one);
       float vv[4];
       getv(jj, vv);
-      Epi::apply(ep, row0 + jj * stride, m0, lane, vv, pre[b]);
+      Epi::apply(ep, row0 + jj * stride, m0, lane, vv, one);
+    }
+  } else {
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int jj = ew + 4 * b;
+      if (jj < nvalid) {
+        float vv[4];
+        getv(jj, vv);
+        Epi::apply(ep, row0 + jj * stride, m0, lane, vv, pre[b]);
+      }
     }
   }
 }

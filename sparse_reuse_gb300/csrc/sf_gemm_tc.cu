@@ -73,6 +73,7 @@ struct Params {
   int splits;  // cluster size along z (1 = no split)
   unsigned* err;
   int pipe;    // pipeline bytes (PIPE_BYTES or PIPE_BYTES_PAIR)
+  int count_early;  // *count is final when the grid starts (written two or more launches back)
 };
 
 template <class Epi>
@@ -99,14 +100,21 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int m0 = m_tile * BM;
   // The first row tile always has rows unless the count is zero; later row
   // tiles learn from the live count whether they have work before they
-  // allocate anything (the decision is uniform over a cluster).
-  const bool lead = n_tile == 0;
-  if (!lead) {
-    pdl_wait();
-    pdl_trigger();
-    const int c0 = p.count ? *p.count : p.dense_count;
-    if (row0 >= c0) return;
+  // allocate anything (the decision is uniform over a cluster).  A count that
+  // is final when the grid starts is read before the dependency wait, so an
+  // empty tile leaves at once instead of holding an SM until the previous
+  // kernel completes: the live tiles still hold the next kernel back.
+  if (n_tile > 0) {
+    if (p.count_early) {
+      if (row0 >= __ldcg(p.count)) return;
+    } else {
+      pdl_wait();
+      pdl_trigger();
+      const int c0 = p.count ? *p.count : p.dense_count;
+      if (row0 >= c0) return;
+    }
   }
+  const bool lead = n_tile == 0 || p.count_early;  // not waited for yet
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
@@ -151,7 +159,12 @@ __global__ void __launch_bounds__(THREADS, 2)
   // them without a split, every S-th one (cluster rank z first) with one
   const int own0 = S > 1 ? z : 0;
   const int n_own = n_rows > own0 ? (n_rows - own0 + S - 1) / S : 0;
-  typename Epi::Pre pre[8];
+  // An epilogue whose rows read global memory issues the reads of the next 32
+  // rows before it applies the current ones (two register sets); a staged
+  // one reads shared memory and needs no look-ahead.
+  constexpr bool kAhead = !epilogue_rolled<Epi>();
+  typename Epi::Pre pre[8], pre2[8];
+  typename Epi::Params epl = ep;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -210,26 +223,41 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     __syncwarp();
   } else if (active) {
-    // the epilogue's global reads for this warp's first rows are issued while
-    // the main loop streams the weights
-    epilogue_prefetch<Epi>(ep, row0 + own0, S, min(32, n_own), m0, ew, lane, pre);
+    // the epilogue's tables (staged) or its global reads for this warp's
+    // first rows are fetched while the main loop streams the weights
+    if constexpr (Epi::kStaged) {
+      Epi::stage(epl, smem + pipe + 256, row0, n_rows, threadIdx.x - 64);
+      named_bar_sync(1, 128);
+    }
+    epilogue_prefetch<Epi>(epl, row0 + own0, S, min(32, n_own), m0, ew, lane, pre);
     go = mbar_wait(tfull, 0, p.err);
     fence_after_sync();
     if (S == 1 && go) {
       float* stage = reinterpret_cast<float*>(smem);
-      for (int j0 = 0; j0 < n_rows; j0 += 32) {
+      auto chunk = [&](int j0, typename Epi::Pre(&cur)[8], typename Epi::Pre(&next)[8]) {
+        const int nxt = min(32, n_rows - j0 - 32);
+        if (kAhead && nxt > 0) epilogue_prefetch<Epi>(epl, row0 + j0 + 32, 1, nxt, m0, ew, lane, next);
         float v[32];
         tmem_ld32(tbase + j0, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) stage[j * STAGE_LD + f] = v[j];
         named_bar_sync(1, 128);
-        if (j0 > 0) epilogue_prefetch<Epi>(ep, row0 + j0, 1, min(32, n_rows - j0), m0, ew, lane, pre);
-        epilogue_apply<Epi>(ep, row0 + j0, 1, min(32, n_rows - j0), m0, ew, lane, pre,
+        if (!kAhead && j0 > 0) epilogue_prefetch<Epi>(epl, row0 + j0, 1, min(32, n_rows - j0), m0, ew, lane, cur);
+        epilogue_apply<Epi>(epl, row0 + j0, 1, min(32, n_rows - j0), m0, ew, lane, cur,
                             [&](int jj, float (&vv)[4]) {
 #pragma unroll
                               for (int c = 0; c < 4; ++c) vv[c] = stage[jj * STAGE_LD + lane + 32 * c];
                             });
         named_bar_sync(1, 128);
+      };
+      for (int j0 = 0; j0 < n_rows; j0 += 64) {
+        chunk(j0, pre, pre2);
+        if (j0 + 32 < n_rows) {
+          if constexpr (kAhead)
+            chunk(j0 + 32, pre2, pre);
+          else
+            chunk(j0 + 32, pre, pre2);
+        }
       }
     }
   }
@@ -262,20 +290,32 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     cluster_sync_all();  // every partial has been delivered
     if (warp >= 2 && go && fits) {
-      for (int t0 = 0; t0 < n_own; t0 += 32) {
-        if (t0 > 0) epilogue_prefetch<Epi>(ep, row0 + own0 + S * t0, S, min(32, n_own - t0), m0, ew, lane, pre);
-        epilogue_apply<Epi>(ep, row0 + own0 + S * t0, S, min(32, n_own - t0), m0, ew, lane, pre,
+      auto part = [&](int t0, typename Epi::Pre(&cur)[8], typename Epi::Pre(&next)[8]) {
+        const int nxt = min(32, n_own - t0 - 32);
+        if (kAhead && nxt > 0)
+          epilogue_prefetch<Epi>(epl, row0 + own0 + S * (t0 + 32), S, nxt, m0, ew, lane, next);
+        if (!kAhead && t0 > 0)
+          epilogue_prefetch<Epi>(epl, row0 + own0 + S * t0, S, min(32, n_own - t0), m0, ew, lane, cur);
+        epilogue_apply<Epi>(epl, row0 + own0 + S * t0, S, min(32, n_own - t0), m0, ew, lane, cur,
                             [&](int jj, float (&vv)[4]) {
                               vv[0] = vv[1] = vv[2] = vv[3] = 0.f;
                               const float* src = buf + (size_t)(t0 + jj) * BM + lane;
+                              // partials in cluster-rank order (a rolled loop: cold code)
+#pragma unroll 1
+                              for (int r = 0; r < S; ++r, src += (size_t)n_slot * BM) {
 #pragma unroll
-                              for (int r = 0; r < 8; ++r) {
-                                if (r < S) {
-#pragma unroll
-                                  for (int cc = 0; cc < 4; ++cc) vv[cc] += src[(size_t)r * n_slot * BM + 32 * cc];
-                                }
+                                for (int cc = 0; cc < 4; ++cc) vv[cc] += src[32 * cc];
                               }
                             });
+      };
+      for (int t0 = 0; t0 < n_own; t0 += 64) {
+        part(t0, pre, pre2);
+        if (t0 + 32 < n_own) {
+          if constexpr (kAhead)
+            part(t0 + 32, pre2, pre);
+          else
+            part(t0 + 32, pre, pre2);
+        }
       }
     }
   }
@@ -400,12 +440,19 @@ template <class Epi>
 cudaError_t launch_tc(const TcGemm& g, const typename Epi::Params& ep, cudaStream_t st) {
   cudaError_t e = set_smem_attr<Epi>();
   if (e != cudaSuccess) return e;
-  // a single-split GEMM with more tiles than SMs runs two CTAs per SM, all in one wave
+  // a single-split GEMM with more tiles than SMs runs two CTAs per SM, all in
+  // one wave; an epilogue's staged tables sit past the barriers and come out
+  // of the pipeline
+  int staged = 0;
+  if constexpr (Epi::kStaged) staged = Epi::stage_bytes(ep);
   const int m_tiles_live = (g.M / tc::BM) * (g.count ? 1 : (g.dense_count + tc::BN - 1) / tc::BN);
-  const int pipe = g.splits == 1 && m_tiles_live > sm_count() ? tc::PIPE_BYTES_PAIR : tc::PIPE_BYTES;
-  tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err, pipe};
+  const int base = g.splits == 1 && m_tiles_live > sm_count() && !staged ? tc::PIPE_BYTES_PAIR : tc::PIPE_BYTES;
+  const int pipe = base - ((staged + 1023) & ~1023);
+  if (tc::stages_for(pipe, 0) < 2) return cudaErrorInvalidValue;
+  tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err, pipe, g.count_early ? 1 : 0};
   return launch_pdl(st, dim3(g.M / tc::BM, (g.max_rows + tc::BN - 1) / tc::BN, g.splits), dim3(tc::THREADS),
-                    (size_t)pipe + 1024 + 256, g.splits, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p, ep);
+                    (size_t)pipe + 1024 + 256 + staged, g.splits, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p,
+                    ep);
 }
 
 }  // namespace

@@ -126,6 +126,7 @@ struct GemmArgs {
   const int32_t* count;    // device row count, or nullptr to use dense_count
   int dense_count;
   int max_rows;            // capacity of X / outputs
+  bool count_early;        // count written two or more launches back (final when the grid starts)
 };
 
 enum EpiKind { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2, kEpiStore = 3 };
@@ -194,6 +195,7 @@ struct TcGemm {
   int max_rows;
   int splits;  // K split over a cluster of this many CTAs (1..6 or 8)
   unsigned* err;
+  bool count_early;  // *count is final before the dependency wait
 };
 bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 int gemm_tc_splits(int M, int K, int n_tiles);
