@@ -297,9 +297,10 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
       tc::tma_load_3d(sk + (HD / 64 + h) * KTILE, &tmV, h * 64, kvh, z, &full[st]);
     }
   };
-  // the prefix keys and values are inputs of the pass
+  // the prefix keys and values are inputs of the pass: every stage is filled
+  // before the wait (with P <= 1024 that is the whole split)
   if (tid == 0)
-    for (int b = 0; b < min(kStages - 1, nblk); ++b) issue(b);
+    for (int b = 0; b < min(kStages, nblk); ++b) issue(b);
   pdl_wait();
   pdl_trigger();
 
@@ -320,7 +321,9 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int b = 0; b < nblk; ++b) {
-    if (tid == 0 && b + kStages - 1 < nblk) issue(b + kStages - 1);  // its stage was freed by the last barrier
+    // block b + kStages - 1 goes to the stage the last barrier freed (the
+    // first kStages blocks were issued before the wait)
+    if (tid == 0 && b >= 1 && b + kStages - 1 < nblk) issue(b + kStages - 1);
     // a wait that gives up raises the error word but does not leave the loop,
     // so every warp keeps reaching the same barriers
     tc::mbar_wait(&full[b % kStages], (b / kStages) & 1, a.err);

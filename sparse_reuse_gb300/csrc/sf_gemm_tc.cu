@@ -74,6 +74,7 @@ struct Params {
   unsigned* err;
   int pipe;    // pipeline bytes (PIPE_BYTES or PIPE_BYTES_PAIR)
   int count_early;  // *count is final when the grid starts (written two or more launches back)
+  int tile;    // rows per row tile (BN; a dense count is split evenly, in multiples of 16)
 };
 
 template <class Epi>
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int m_tile = blockIdx.x, n_tile = blockIdx.y;
   const int S = p.splits;
   const int z = S > 1 ? (int)cluster_ctarank() : 0;
-  const int row0 = n_tile * BN;
+  const int row0 = n_tile * p.tile;
   const int nk = p.K / BK;
   const int kb0 = (int)((long long)z * nk / S);
   const int kb1 = (int)((long long)(z + 1) * nk / S);
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   const int count = p.count ? *p.count : p.dense_count;
   const bool active = row0 < count;  // uniform over the cluster
-  const int n_rows = active ? min(BN, count - row0) : 0;
+  const int n_rows = active ? min(p.tile, count - row0) : 0;
   const int n_mma = (n_rows + 15) & ~15;
   const int n_chunks = (n_rows + RC - 1) / RC;
   const int nst = stages_for(pipe, n_chunks);  // uniform over the cluster
@@ -449,8 +450,15 @@ cudaError_t launch_tc(const TcGemm& g, const typename Epi::Params& ep, cudaStrea
   const int base = g.splits == 1 && m_tiles_live > sm_count() && !staged ? tc::PIPE_BYTES_PAIR : tc::PIPE_BYTES;
   const int pipe = base - ((staged + 1023) & ~1023);
   if (tc::stages_for(pipe, 0) < 2) return cudaErrorInvalidValue;
-  tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err, pipe, g.count_early ? 1 : 0};
-  return launch_pdl(st, dim3(g.M / tc::BM, (g.max_rows + tc::BN - 1) / tc::BN, g.splits), dim3(tc::THREADS),
+  // a dense row count is split into equal row tiles (multiples of 16, the
+  // MMA's N step), so no tile carries a short remainder
+  int tile = tc::BN, n_tiles = (g.max_rows + tc::BN - 1) / tc::BN;
+  if (!g.count && g.dense_count > 0) {
+    n_tiles = (g.dense_count + tc::BN - 1) / tc::BN;
+    tile = ((g.dense_count + n_tiles - 1) / n_tiles + 15) & ~15;
+  }
+  tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err, pipe, g.count_early ? 1 : 0, tile};
+  return launch_pdl(st, dim3(g.M / tc::BM, n_tiles, g.splits), dim3(tc::THREADS),
                     (size_t)pipe + 1024 + 256 + staged, g.splits, tc::gemm_tc_kernel<Epi>, *g.tmA, *g.tmB, p,
                     ep);
 }
