@@ -39,12 +39,18 @@ struct Splits {
 };
 
 // Tensor-core path: the split count is fixed on the host from the prefix
-// length alone (at most 128 keys per CTA), so the split CTAs of a query tile
-// form a cluster of exactly that size.
-constexpr int kKeysPerSplit = 128;
+// length alone, so the split CTAs of a query tile form a cluster of exactly
+// that size.  Up to 512 keys a split is two 64-key blocks (more CTAs for a
+// short, latency-bound job); longer prefixes take four blocks per split,
+// which halves the partial states the cluster exchanges and merges.
+__host__ __device__ __forceinline__ int keys_per_split(int P) { return P <= 512 ? 128 : 256; }
+// K/V stages of the mma.sync prefix kernel: every block of a split is in
+// flight before the dependency wait.
+__host__ __device__ __forceinline__ int mma_prefix_stages(int P) { return keys_per_split(P) / 64; }
 __host__ __device__ __forceinline__ Splits fixed_splits(int P) {
   if (P <= 0) return {0, 0};
-  int S = (P + kKeysPerSplit - 1) / kKeysPerSplit;
+  const int kps = keys_per_split(P);
+  int S = (P + kps - 1) / kps;
   S = S < 1 ? 1 : (S > kMaxSplits ? kMaxSplits : S);
   const int len = (((P + S - 1) / S) + kKB - 1) / kKB * kKB;
   return {(P + len - 1) / len, len};
@@ -232,20 +238,18 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HD / 16][4], const b
 // Prefix partials: CTA = (64 query vectors of one request and KV head, one
 // split of the prefix).  Query vector v of the request is recompute slot
 // off_r + v / G, query head kvh * G + v % G.  K/V blocks of 64 keys stream
-// through a kStages-deep ring of TMA loads (one (64-dim, 1-head, 64-key) box
+// through a STAGES-deep ring of TMA loads (one (64-dim, 1-head, 64-key) box
 // per 64-dim half); the split CTAs of a query tile form one cluster (along z):
 // after their streaming loops every CTA sends its partial state (max,
 // denominator, unnormalised output) of each query row to the CTA that owns
 // the row, and each owner merges the S states in rank order and writes one
 // merged state per query.
-constexpr int kStages = 2;
-
-template <int HD>
+template <int HD, int STAGES>
 constexpr int prefix_smem_bytes() {
-  return kStages * 2 * (HD / 64) * (kKB * 128) + kQT * (HD + 8) * 2 + 64 + 1024;
+  return STAGES * 2 * (HD / 64) * (kKB * 128) + kQT * (HD + 8) * 2 + 64 + 1024;
 }
 
-template <int HD>
+template <int HD, int STAGES>
 __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ CUtensorMap tmK,
                                                        const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
   constexpr int LD = HD + 8;
@@ -255,8 +259,8 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  bf16* sQ = reinterpret_cast<bf16*>(base + kStages * STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + kStages * STAGE + kQT * LD * 2);
+  bf16* sQ = reinterpret_cast<bf16*>(base + STAGES * STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * STAGE + kQT * LD * 2);
   float* xbuf = reinterpret_cast<float*>(base);  // exchange area, reused after the loop
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // grid: x = (request, KV head), y = query tile, z = split; the first query
@@ -282,12 +286,12 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
 
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) tc::mbar_init(&full[st], 1);
+    for (int st = 0; st < STAGES; ++st) tc::mbar_init(&full[st], 1);
     tc::fence_barrier_init();
   }
   __syncthreads();
   auto issue = [&](int b) {  // thread 0: K and V of key block b into its stage
-    const int st = b % kStages;
+    const int st = b % STAGES;
     unsigned char* sk = base + st * STAGE;
     const int z = r * a.P + k_lo + b * kKB;
     tc::mbar_expect_tx(&full[st], STAGE);
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   // the prefix keys and values are inputs of the pass: every stage is filled
   // before the wait (with P <= 1024 that is the whole split)
   if (tid == 0)
-    for (int b = 0; b < min(kStages, nblk); ++b) issue(b);
+    for (int b = 0; b < min(STAGES, nblk); ++b) issue(b);
   pdl_wait();
   pdl_trigger();
 
@@ -321,13 +325,13 @@ __global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ C
   for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int b = 0; b < nblk; ++b) {
-    // block b + kStages - 1 goes to the stage the last barrier freed (the
-    // first kStages blocks were issued before the wait)
-    if (tid == 0 && b >= 1 && b + kStages - 1 < nblk) issue(b + kStages - 1);
+    // block b + STAGES - 1 goes to the stage the last barrier freed (the
+    // first STAGES blocks were issued before the wait)
+    if (tid == 0 && b >= 1 && b + STAGES - 1 < nblk) issue(b + STAGES - 1);
     // a wait that gives up raises the error word but does not leave the loop,
     // so every warp keeps reaching the same barriers
-    tc::mbar_wait(&full[b % kStages], (b / kStages) & 1, a.err);
-    const unsigned char* sk = base + (b % kStages) * STAGE;
+    tc::mbar_wait(&full[b % STAGES], (b / STAGES) & 1, a.err);
+    const unsigned char* sk = base + (b % STAGES) * STAGE;
     float sc[kKB / 8][4];
     qk_scores_sw<HD>(sc, qf, sk, lane);
     const int kb0 = k_lo + b * kKB;
@@ -1139,8 +1143,11 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
     cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcLayout<HD>::BYTES);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_prefix_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               prefix_smem_bytes<HD>());
+      e = cudaFuncSetAttribute(attn_prefix_mma<HD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               prefix_smem_bytes<HD, 2>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_prefix_mma<HD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               prefix_smem_bytes<HD, 4>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_mma<HD, kKB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
@@ -1165,8 +1172,12 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
     } else {
       const Splits sp = fixed_splits(a.P);
       dim3 grid(a.R * a.nkv, (a.Bp * a.L * G + kQT - 1) / kQT, sp.S);
-      lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD>(), sp.S, attn_prefix_mma<HD>, tmK,
-                          tmV, a));
+      if (mma_prefix_stages(a.P) == 2)
+        lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD, 2>(), sp.S, attn_prefix_mma<HD, 2>,
+                            tmK, tmV, a));
+      else
+        lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD, 4>(), sp.S, attn_prefix_mma<HD, 4>,
+                            tmK, tmV, a));
     }
     lc.after(SF_K_ATTN_PREFIX);
   }
