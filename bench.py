@@ -84,20 +84,14 @@ def pass_work(cfg, rc_counts):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
-# from the committed ncu captures of the current kernels: profiles/
-# gemm_tc_1p5b_2layer.md, gemm_attn_14b_2layer.md (GEMMs) and
-# attention_tc_14b_2layer.md (tcgen05 prefix attention).  A kernel
-# changed since its capture has no entry (traffic is then reported as null).
+# from the committed ncu capture of the current kernels (profiles/
+# gemm_tc_1p5b_2layer.md).  A kernel changed since its capture has no entry
+# (traffic is then reported as null).
 NCU_TRAFFIC = {
-    ("1.5b", "gemm_gateup"): 55.31e6,
-    ("1.5b", "gemm_down"): 28.72e6,
-    ("1.5b", "gemm_o"): 7.52e6,
-    ("1.5b", "gemm_qkv"): 6.58e6,
-    ("14b", "gemm_gateup"): 288.35e6 + 5.67e6,
-    ("14b", "gemm_o"): 133.12e6 + 10.63e6,
-    ("14b", "gemm_down"): 148.69e6 + 3.19e6,
-    ("14b", "gemm_qkv"): 76.13e6 + 1.71e6,
-    ("14b", "attn_prefix"): 69.80e6 + 1.82e6,
+    ("1.5b", "gemm_gateup"): 55.29e6,
+    ("1.5b", "gemm_down"): 28.70e6,
+    ("1.5b", "gemm_o"): 7.57e6,
+    ("1.5b", "gemm_qkv"): 6.55e6,
 }
 
 
