@@ -30,7 +30,8 @@ extern "C" {
  *   splits     1..8, at most K/64: K is split over a cluster of this
  *              many CTAs per output tile, whose partial sums are added in
  *              cluster-rank order in shared memory (no workspace).
- *   err        device uint32 error word (bit 32 = a bounded wait gave up) or NULL.
+ *   err        device uint32 error word or NULL: the kernel ORs in 4 for a bad
+ *              argument or index and 32 when a bounded wait gave up.
  * Errors: SF_ERR_INVALID_ARG (null operand, bad M/K/splits/ldy, unaligned
  * pointer), SF_ERR_CUDA (descriptor encoding or launch failure).
  * Asynchronous; the buffers must stay valid until the stream reaches it. */
