@@ -171,11 +171,12 @@ constexpr bool epilogue_rolled() {
 template <class Epi>
 __device__ __forceinline__ void epilogue_prefetch(const typename Epi::Params& ep, int row0, int stride, int nvalid,
                                                   int m0, int ew, int lane, typename Epi::Pre (&pre)[8]) {
-  if constexpr (epilogue_rolled<Epi>()) return;
+  if constexpr (!epilogue_rolled<Epi>()) {  // a rolled epilogue reads each row just before use
 #pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    const int jj = ew + 4 * b;
-    if (jj < nvalid) Epi::prefetch(ep, row0 + jj * stride, m0, lane, pre[b]);
+    for (int b = 0; b < 8; ++b) {
+      const int jj = ew + 4 * b;
+      if (jj < nvalid) Epi::prefetch(ep, row0 + jj * stride, m0, lane, pre[b]);
+    }
   }
 }
 

@@ -18,7 +18,7 @@
 namespace sf {
 namespace {
 
-constexpr int kGateThreads = 256;
+constexpr int kGateThreads = 256;  // every kernel of this file
 
 // One row of the layer input in fp32, 4 features at column c4 * 4.
 template <bool kLayer0, typename TIn>
@@ -131,7 +131,7 @@ __device__ void compact_and_resolve(const GateArgs& a, uint8_t* flags, int* slot
 // parent row, then reduces and stores them, so all its loads are in flight at
 // once; long rows (VEC == 0) are streamed in a loop at full occupancy.
 template <bool kLayer0, typename TIn, int VEC>
-__global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ GateArgs a) {
+__global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constant__ GateArgs a) {
   __shared__ float red[32];
   __shared__ int tmp[32];
   __shared__ bool is_last;
@@ -255,7 +255,7 @@ constexpr unsigned long long kDoneWaitNs = 2000000000ull;  // a wait that gives 
 // Short rows (VEC > 0) stay in registers; long rows (VEC == 0) are kept in
 // dynamic shared memory until their slot is known.
 template <bool kLayer0, typename TIn, int VEC, typename TAct>
-__global__ void __launch_bounds__(256) gate_norm_kernel(const __grid_constant__ GateArgs a) {
+__global__ void __launch_bounds__(kGateThreads) gate_norm_kernel(const __grid_constant__ GateArgs a) {
   __shared__ float red[32];
   __shared__ int tmp[32];
   __shared__ int s_fold, s_last, s_slot;
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(256) gate_norm_kernel(const __grid_constant__ 
 // RMSNorm of rows rc[g] (or g when rc is null), g < count, gathered into a
 // dense [count][d] activation matrix.
 template <typename TAct>
-__global__ void __launch_bounds__(256) rmsnorm_gather_kernel(const float* X, const int32_t* rc, const int32_t* count_ptr,
+__global__ void __launch_bounds__(kGateThreads) rmsnorm_gather_kernel(const float* X, const int32_t* rc, const int32_t* count_ptr,
                                                              int max_rows, const float* gain, float eps, TAct* out,
                                                              int d, unsigned* err) {
   __shared__ float red[32];
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(256) rmsnorm_gather_kernel(const float* X, con
 
 // Last layer's residual add for every row, cast to the output type.
 template <typename TOut>
-__global__ void __launch_bounds__(256) final_residual_kernel(const float* h, const float* f, const int32_t* rcslot,
+__global__ void __launch_bounds__(kGateThreads) final_residual_kernel(const float* h, const float* f, const int32_t* rcslot,
                                                              TOut* out, float* dbg, int T, int d, unsigned* epoch,
                                                              unsigned* err) {
   pdl_wait();
@@ -496,9 +496,9 @@ cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16) {
   // parent); longer rows: the streaming loop
   lc.before(SF_K_GATE);
   if (d4 <= 512)
-    lc.check(launch_gate_vec<2>(lc, a, in_bf16, 256, dyn));
+    lc.check(launch_gate_vec<2>(lc, a, in_bf16, kGateThreads, dyn));
   else
-    lc.check(launch_gate_vec<0>(lc, a, in_bf16, 256, dyn));
+    lc.check(launch_gate_vec<0>(lc, a, in_bf16, kGateThreads, dyn));
   lc.after(SF_K_GATE);
   return lc.err;
 }
@@ -517,7 +517,7 @@ cudaError_t launch_gate_norm_vec(Launch& lc, const GateArgs& a, int bf16) {
     const cudaError_t e = cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(lc.st, dim3(a.T), dim3(256), dyn, 1, k0, a);
+  return launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, k0, a);
 }
 
 }  // namespace
@@ -541,10 +541,10 @@ cudaError_t launch_rmsnorm_gather(Launch& lc, int fam, const float* X, const int
   lc.before(fam);
   const int grid = grid_rows(max_rows);
   if (act_bf16)
-    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, rmsnorm_gather_kernel<__nv_bfloat16>, X, rc, count,
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(kGateThreads), 0, 1, rmsnorm_gather_kernel<__nv_bfloat16>, X, rc, count,
                         max_rows, gain, eps, (__nv_bfloat16*)out, d, err));
   else
-    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, rmsnorm_gather_kernel<float>, X, rc, count, max_rows,
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(kGateThreads), 0, 1, rmsnorm_gather_kernel<float>, X, rc, count, max_rows,
                         gain, eps, (float*)out, d, err));
   lc.after(fam);
   return lc.err;
@@ -555,10 +555,10 @@ cudaError_t launch_final_residual(Launch& lc, const float* h, const float* f, co
   lc.before(SF_K_RESIDUAL);
   const int grid = grid_rows(T);
   if (out_bf16)
-    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, final_residual_kernel<__nv_bfloat16>, h, f, rcslot,
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(kGateThreads), 0, 1, final_residual_kernel<__nv_bfloat16>, h, f, rcslot,
                         (__nv_bfloat16*)out, dbg, T, d, epoch, err));
   else
-    lc.check(launch_pdl(lc.st, dim3(grid), dim3(256), 0, 1, final_residual_kernel<float>, h, f, rcslot, (float*)out,
+    lc.check(launch_pdl(lc.st, dim3(grid), dim3(kGateThreads), 0, 1, final_residual_kernel<float>, h, f, rcslot, (float*)out,
                         dbg, T, d, epoch, err));
   lc.after(SF_K_RESIDUAL);
   return lc.err;
