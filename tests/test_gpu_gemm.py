@@ -58,6 +58,14 @@ def test_dense_count_and_long_k(sf):
     _run(sf, 1536, 1536, 288, 288, 4, on_device=False)
 
 
+@pytest.mark.parametrize("count", [257, 300, 513])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_dense_counts_split_into_equal_tiles(sf, count, splits):
+    # a host-known count is cut into ceil(count / 256) tiles of equal size (a
+    # multiple of 16); the last tile's row boxes reach past rows_cap (zero fill)
+    _run(sf, 256, 512, count, count, splits, on_device=False, seed=4)
+
+
 def test_split_results_are_deterministic(sf):
     a = _run(sf, 256, 2048, 288, 288, 6, seed=3)
     b = _run(sf, 256, 2048, 288, 288, 6, seed=3)
