@@ -113,10 +113,13 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
  *   src        device int32 [n_layers, R, B+1, L]: resolved source branch of
  *              every position (the branch itself when recomputed) or NULL.
  *   rc_count   device int32 [n_layers]: size of the recompute set, or NULL.
- * Output buffers are caller-owned and must not alias the inputs.
- * Errors (returned before anything is enqueued): SF_ERR_INVALID_ARG,
- * SF_ERR_SHAPE, SF_ERR_TREE; SF_ERR_DEVICE_ASSERT if an earlier pass on this
- * context tripped a device-side check; SF_ERR_CUDA on a launch failure. */
+ * Output buffers are caller-owned and must not alias the inputs.  hidden_in,
+ * hidden_out, prefix_k and prefix_v start on a 16-byte boundary (rows are
+ * moved with 16-byte vectors and TMA), src and rc_count on a 4-byte one.
+ * Errors (returned before anything is enqueued): SF_ERR_INVALID_ARG (also for
+ * a misaligned pointer), SF_ERR_SHAPE, SF_ERR_TREE; SF_ERR_DEVICE_ASSERT if an
+ * earlier pass on this context tripped a device-side check; SF_ERR_CUDA on a
+ * launch failure. */
 sf_status sf_verify(sf_ctx* ctx, void* stream, const void* hidden_in, const int32_t* parent,
                     const void* prefix_k, const void* prefix_v, int R, int B, int P, float delta,
                     void* hidden_out, uint8_t* fold_mask, int32_t* src, int32_t* rc_count);
@@ -126,7 +129,9 @@ sf_status sf_verify(sf_ctx* ctx, void* stream, const void* hidden_in, const int3
  *                stream entering every layer, then the final fp32 output.
  *   rc_rows      device int32 [n_layers, R*(B+1)*L]: the compacted recompute
  *                list of every layer (ascending row ids (r*(B+1)+i)*L+n; the
- *                tail past rc_count is left untouched). */
+ *                tail past rc_count is left untouched).
+ * layer_hidden starts on a 16-byte boundary, rc_rows on a 4-byte one
+ * (SF_ERR_INVALID_ARG otherwise). */
 sf_status sf_set_debug(sf_ctx* ctx, float* layer_hidden, int32_t* rc_rows);
 
 /* Wait for the context's work on `stream` to finish and report a device-side

@@ -52,20 +52,23 @@ sf_status sfk_gemm_bf16(void* stream, const void* X, int rows_cap, const void* W
  * until the process exits.
  *
  *   hidden    device [R, B+1, L, d] in dtype (SF_F32 or SF_BF16): the block's
- *             layer-0 input; d a multiple of 4, rows 16-byte aligned.
+ *             layer-0 input; d a multiple of 4, read as 4-element vectors:
+ *             the base 16-byte aligned for SF_F32, 8-byte for SF_BF16.
  *   parent    HOST int32 [R, B+1], same rules as sf_verify.
  *   delta     >= 0 and finite; 0 means nothing folds.
  * Outputs (device, caller-owned, all required), T = R * (B+1) * L:
- *   H_out     fp32 [T, d]: the input converted to fp32.
+ *   H_out     fp32 [T, d], 16-byte aligned: the input converted to fp32.
  *   fold      uint8 [T]: 1 = folded.
  *   rc        int32 [T]: ascending recompute row ids (r*(B+1)+i)*L+n; the
  *             first *rc_count entries are written.
  *   rcslot    int32 [T]: index in rc of each row's resolved source.
  *   src       int32 [T]: resolved source branch of each row.
  *   rc_count  int32 [1]: size of the recompute set.
+ * The int32 outputs start on a 4-byte boundary.
  * Limits (SF_ERR_SHAPE beyond them): T <= 8192, R * (B+1) <= 1024, B+1 <= 127.
- * Errors returned before anything is enqueued: SF_ERR_INVALID_ARG,
- * SF_ERR_SHAPE, SF_ERR_TREE; SF_ERR_CUDA if the set-up or launch fails.
+ * Errors returned before anything is enqueued: SF_ERR_INVALID_ARG (also for
+ * a misaligned pointer), SF_ERR_SHAPE, SF_ERR_TREE; SF_ERR_CUDA if the set-up
+ * or launch fails.
  *
  * The first call on a device (with that device current) looks up the
  * array's device address; make that first call before any stream capture.

@@ -43,6 +43,9 @@ sf_status fail(sf_ctx* c, sf_status st, const char* fmt, ...) {
   return st;
 }
 
+// A non-null pointer that does not start on an `align`-byte boundary.
+bool misaligned(const void* p, uintptr_t align) { return p && (reinterpret_cast<uintptr_t>(p) & (align - 1)); }
+
 template <typename T>
 cudaError_t dalloc(T** p, size_t bytes) {
   void* q = nullptr;
@@ -388,6 +391,11 @@ sf_status sf_verify(sf_ctx* c, void* stream, const void* hidden_in, const int32_
     return fail(c, SF_ERR_SHAPE, "R=%d B=%d P=%d beyond capacity (%d, %d, %d)", R, B, P, c->s.max_requests,
                 c->s.max_branches - 1, c->s.max_prefix);
   if (P > 0 && (!prefix_k || !prefix_v)) return fail(c, SF_ERR_INVALID_ARG, "null prefix K/V with P > 0");
+  // rows move as 16-byte vectors (and the prefix through TMA): a misaligned
+  // buffer is refused here rather than met by a kernel
+  if (misaligned(hidden_in, 16) || misaligned(hidden_out, 16) || misaligned(prefix_k, 16) ||
+      misaligned(prefix_v, 16) || misaligned(src, 4) || misaligned(rc_count, 4))
+    return fail(c, SF_ERR_INVALID_ARG, "hidden and prefix buffers need 16-byte alignment, src/rc_count 4-byte");
   const int Bp = B + 1;
   for (int r = 0; r < R; ++r) {
     if (parent[r * Bp] != -1) return fail(c, SF_ERR_TREE, "request %d: parent[0] must be -1", r);
@@ -483,6 +491,8 @@ sf_status sf_verify(sf_ctx* c, void* stream, const void* hidden_in, const int32_
 
 sf_status sf_set_debug(sf_ctx* c, float* layer_hidden, int32_t* rc_rows) {
   if (!c) return SF_ERR_INVALID_ARG;
+  if (misaligned(layer_hidden, 16) || misaligned(rc_rows, 4))
+    return fail(c, SF_ERR_INVALID_ARG, "layer_hidden needs 16-byte alignment, rc_rows 4-byte");
   c->dbg_hidden = layer_hidden;
   c->dbg_rc = rc_rows;
   return SF_OK;

@@ -628,6 +628,11 @@ extern "C" sf_status sfk_gate_noalloc(void* stream, const void* hidden, int dtyp
   if ((dtype != SF_F32 && dtype != SF_BF16) || R < 1 || B < 0 || L < 1 || d <= 0 || d % 4 != 0 ||
       !std::isfinite(delta) || delta < 0.f)
     return SF_ERR_INVALID_ARG;
+  // rows are read as 4-element vectors and H_out is written as float4
+  auto misaligned = [](const void* p, uintptr_t align) { return (reinterpret_cast<uintptr_t>(p) & (align - 1)) != 0; };
+  if (misaligned(hidden, dtype == SF_F32 ? 16 : 8) || misaligned(H_out, 16) || misaligned(rc, 4) ||
+      misaligned(rcslot, 4) || misaligned(src, 4) || misaligned(rc_count, 4))
+    return SF_ERR_INVALID_ARG;
   const int Bp = B + 1;
   if (Bp > 127 || (long)R * Bp > kMaxTreeSlots || (long)R * Bp * L > kMaxRows) return SF_ERR_SHAPE;
   for (int r = 0; r < R; ++r) {

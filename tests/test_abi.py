@@ -69,3 +69,35 @@ def test_create_rejects_null_weights(lib):
     w = (lib.SfLayerWeights * 1)(lib.SfLayerWeights(*([1] * 8 + [0])))
     assert lib.lib.sf_create(ctypes.byref(_shapes(lib)), w, ctypes.byref(ctx)) == lib.SF_ERR_INVALID_ARG
     assert lib.lib.sf_create(None, w, ctypes.byref(ctx)) == lib.SF_ERR_INVALID_ARG
+
+
+def _gate_noalloc(lib, hidden, dtype, parent, h_out, rc, delta=0.1, R=1, B=2):
+    par = (ctypes.c_int32 * parent.size)(*parent.ravel().tolist())
+    # device addresses are never dereferenced: every case is refused on the host
+    return lib.lib.sfk_gate_noalloc(None, hidden, dtype, par, R, B, 32, 256, delta, h_out, 16, rc, 16, 16, 16)
+
+
+def test_noalloc_gate_host_checks_before_any_device_work(lib):
+    import numpy as np
+    good, bad_tree = np.array([[-1, 0, 1]], np.int32), np.array([[0, 0, 1]], np.int32)
+    assert _gate_noalloc(lib, 16, lib.SF_F32, bad_tree, 16, 16) == lib.SF_ERR_TREE
+    assert _gate_noalloc(lib, 16, lib.SF_F32, good, 16, 16, delta=float("nan")) == lib.SF_ERR_INVALID_ARG
+    assert _gate_noalloc(lib, 16, lib.SF_F32, np.tile(good, (100, 1)), 16, 16, R=100) == lib.SF_ERR_SHAPE
+    # misaligned buffers are refused before the tree is looked at: fp32 rows
+    # need 16 bytes, bf16 rows 8, H_out 16, the int32 outputs 4
+    for dtype, hidden, h_out, rc in ((lib.SF_F32, 24, 16, 16), (lib.SF_BF16, 20, 16, 16),
+                                     (lib.SF_F32, 16, 24, 16), (lib.SF_F32, 16, 16, 18)):
+        assert _gate_noalloc(lib, hidden, dtype, bad_tree, h_out, rc) == lib.SF_ERR_INVALID_ARG
+    # bf16 rows 8-byte aligned pass the alignment check (and stop at the tree)
+    assert _gate_noalloc(lib, 24, lib.SF_BF16, bad_tree, 16, 16) == lib.SF_ERR_TREE
+
+
+def test_gemm_host_checks_before_any_device_work(lib):
+    f = lib.lib.sfk_gemm_bf16
+    # M not a multiple of 128, K not a multiple of 64, a cluster larger than 8,
+    # a misaligned operand: all refused without a launch
+    assert f(None, 16, 64, 16, 100, 64, None, 1, 16, 100, 1, None) == lib.SF_ERR_INVALID_ARG
+    assert f(None, 16, 64, 16, 128, 96, None, 1, 16, 128, 1, None) == lib.SF_ERR_INVALID_ARG
+    assert f(None, 16, 64, 16, 128, 1024, None, 1, 16, 128, 9, None) == lib.SF_ERR_INVALID_ARG
+    assert f(None, 24, 64, 16, 128, 1024, None, 1, 16, 128, 1, None) == lib.SF_ERR_INVALID_ARG
+    assert f(None, 16, 64, 24, 128, 1024, None, 1, 16, 128, 1, None) == lib.SF_ERR_INVALID_ARG

@@ -182,7 +182,15 @@ def test_argument_and_tree_errors_launch_nothing():
     wl = _wl(cfg)
     ctx = sf.from_config(cfg, wl.weights)
     before = ctx.stats()["kernel_launches"]
+    out = torch.empty_like(wl.hidden)
+    # a misaligned buffer comes with an invalid tree, which is checked later:
+    # the alignment check must be the one that answers, and if it did not the
+    # tree check would still refuse the call before any launch
+    bad_tree = np.array([[0, 0, 1]])
     bad = [
+        (dict(hidden=wl.hidden.data_ptr() + 4, parent=bad_tree), sf.SF_ERR_INVALID_ARG),
+        (dict(out=out.data_ptr() + 8, parent=bad_tree), sf.SF_ERR_INVALID_ARG),
+        (dict(pk=wl.prefix_k.data_ptr() + 4, parent=bad_tree), sf.SF_ERR_INVALID_ARG),
         (dict(parent=np.array([[0, 0, 1]])), sf.SF_ERR_TREE),
         (dict(parent=np.array([[-1, 1, 1]])), sf.SF_ERR_TREE),
         (dict(parent=np.array([[-1, 0, 3]])), sf.SF_ERR_TREE),
@@ -193,14 +201,19 @@ def test_argument_and_tree_errors_launch_nothing():
         (dict(P=cfg.prefix_len + 1), sf.SF_ERR_SHAPE),
         (dict(hidden=0), sf.SF_ERR_INVALID_ARG),
     ]
-    out = torch.empty_like(wl.hidden)
     for kw, status in bad:
         parent = kw.get("parent", wl.parents)
         with pytest.raises(sf.SpecFoldError) as ei:
-            sf.sf_verify(ctx.ctx, None, kw.get("hidden", wl.hidden.data_ptr()), parent, wl.prefix_k.data_ptr(),
-                         wl.prefix_v.data_ptr(), parent.shape[0], parent.shape[1] - 1, kw.get("P", cfg.prefix_len),
-                         kw.get("delta", 0.1), out.data_ptr())
+            sf.sf_verify(ctx.ctx, None, kw.get("hidden", wl.hidden.data_ptr()), parent,
+                         kw.get("pk", wl.prefix_k.data_ptr()), wl.prefix_v.data_ptr(), parent.shape[0],
+                         parent.shape[1] - 1, kw.get("P", cfg.prefix_len), kw.get("delta", 0.1),
+                         kw.get("out", out.data_ptr()))
         assert ei.value.status == status, (kw, ei.value)
+    # the debug capture refuses a misaligned dump buffer (it only records pointers)
+    dump = torch.empty((cfg.n_layers + 1) * wl.hidden.numel() + 4, device="cuda")
+    with pytest.raises(sf.SpecFoldError) as ei:
+        sf.sf_set_debug(ctx.ctx, dump.data_ptr() + 4, None)
+    assert ei.value.status == sf.SF_ERR_INVALID_ARG
     assert ctx.stats()["kernel_launches"] == before
     # R = 0 is an empty pass
     sf.sf_verify(ctx.ctx, None, wl.hidden.data_ptr(), np.zeros((0, 3), np.int32), None, None, 0, 2, 0, 0.1,

@@ -93,3 +93,10 @@ def test_noalloc_gate_rejects_bad_arguments(sf):
     with pytest.raises(sf.SpecFoldError) as e:
         sf.sfk_gate_noalloc(None, 16, 0, p, 1, 2, 32, 256, -1.0, 16, 16, 16, 16, 16, 16)
     assert e.value.status == sf.SF_ERR_INVALID_ARG
+    # misaligned buffers (with a tree that is refused later, so nothing can
+    # launch): fp32 rows need 16 bytes, bf16 rows 8, H_out 16, int32 outputs 4
+    bad_tree = np.array([[0, 0, 1]], np.int32)
+    for dtype, hidden, h_out, rc in ((0, 24, 16, 16), (1, 20, 16, 16), (0, 16, 24, 16), (0, 16, 16, 18)):
+        with pytest.raises(sf.SpecFoldError) as e:
+            sf.sfk_gate_noalloc(None, hidden, dtype, bad_tree, 1, 2, 32, 256, 0.1, h_out, 16, rc, 16, 16, 16)
+        assert e.value.status == sf.SF_ERR_INVALID_ARG, (dtype, hidden, h_out, rc)
