@@ -84,8 +84,8 @@ def pass_work(cfg, rc_counts):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
-# from the committed ncu capture of the current kernels (profiles/
-# gemm_tc_1p5b_2layer.md).  A kernel changed since its capture has no entry
+# from the committed ncu capture of the current kernels (the 1.5B GEMM
+# summary under profiles/).  A kernel changed since its capture has no entry
 # (traffic is then reported as null).
 NCU_TRAFFIC = {
     ("1.5b", "gemm_gateup"): 55.29e6,
