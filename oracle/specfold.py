@@ -335,6 +335,52 @@ def corrected_attention(q: np.ndarray, K_par: np.ndarray, V_par: np.ndarray,
 
 
 # --------------------------------------------------------------------------
+# Verification head: final RMSNorm, LM head, greedy tokens, draft acceptance
+# ([SF] §1, §2.2: a draft whose state matches supplies logits that skip later
+# denoising passes; App. B: the LM head runs outside the layer kernels)
+# --------------------------------------------------------------------------
+
+def lm_head_logits(h_rows: np.ndarray, final_norm: np.ndarray, W_lm: np.ndarray, eps: float) -> np.ndarray:
+    """Logits of output rows [..., d]: RMSNorm with the final gain, then the
+    LM head W_lm [d, V] (row-major [in, out] like every other weight)."""
+    return rms_norm(h_rows, final_norm, eps) @ np.asarray(W_lm, F64)
+
+
+def greedy_tokens(logits: np.ndarray) -> np.ndarray:
+    """Greedy prediction per row: the index of the largest logit, the lowest
+    such index on a tie."""
+    return np.argmax(np.asarray(logits), axis=-1)
+
+
+def accept_drafts(tokens: np.ndarray, parent: Sequence[int], pred: np.ndarray):
+    """Draft acceptance of one request.
+
+    tokens [B+1, L]: every branch's block tokens; pred [B+1, L]: every
+    branch's greedy prediction at every position.  Reading (the pages say only
+    that a matching draft can supply logits for later passes): draft i matches
+    iff its parent matches and every position where its tokens differ from
+    its parent's holds the parent's greedy prediction there.  The main branch
+    always matches.  Returns (accepted [B+1] bool, chosen): chosen is the
+    deepest matching branch, the lowest index among equally deep ones."""
+    tokens = np.asarray(tokens)
+    pred = np.asarray(pred)
+    Bp = tokens.shape[0]
+    accepted = np.zeros(Bp, dtype=bool)
+    depth = np.zeros(Bp, dtype=np.int64)
+    accepted[0] = True
+    for i in range(1, Bp):                      # index order is topological
+        p = parent[i]
+        depth[i] = depth[p] + 1
+        changed = tokens[i] != tokens[p]
+        accepted[i] = accepted[p] and bool(np.all(tokens[i][changed] == pred[p][changed]))
+    chosen = 0
+    for i in range(Bp):
+        if accepted[i] and depth[i] > depth[chosen]:
+            chosen = i
+    return accepted, chosen
+
+
+# --------------------------------------------------------------------------
 # Brute force with scalar loops, for tiny inputs only
 # --------------------------------------------------------------------------
 

@@ -240,3 +240,50 @@ def test_paper_style_correction_equals_direct():
     # nothing changed -> the parent's own attention
     got0 = oracle.corrected_attention(q, Kp, Vp, Kp, Vp, np.zeros(S, bool))
     np.testing.assert_allclose(got0, oracle.attention(q[None], Kp, Vp)[0], rtol=1e-13)
+
+
+# ---------------------------------------------------------------- verification head
+
+def test_acceptance_golden():
+    """Hand-worked draft acceptance on a 6-branch tree (tests/golden/acceptance.json)."""
+    import json
+    g = json.load(open(os.path.join(GOLD, "acceptance.json")))
+    for case in g["cases"]:
+        acc, chosen = oracle.accept_drafts(np.array(g["tokens"]), g["parent"], np.array(case["pred"]))
+        assert acc.astype(int).tolist() == case["accepted"]
+        assert chosen == case["chosen"]
+
+
+def test_acceptance_invariants():
+    """Main always matches; a child equal to its parent matches iff the parent
+    does; a child of a rejected draft is rejected whatever it holds."""
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        Bp, L = 7, 8
+        parent = [-1] + [int(rng.integers(0, i)) for i in range(1, Bp)]
+        tokens = rng.integers(0, 4, size=(Bp, L))
+        pred = rng.integers(0, 4, size=(Bp, L))
+        for i in range(1, Bp):                      # some children copy their parent
+            if rng.random() < 0.4:
+                tokens[i] = tokens[parent[i]]
+        acc, chosen = oracle.accept_drafts(tokens, parent, pred)
+        assert acc[0] and acc[chosen]
+        for i in range(1, Bp):
+            if not acc[parent[i]]:
+                assert not acc[i]
+            if np.array_equal(tokens[i], tokens[parent[i]]):
+                assert acc[i] == acc[parent[i]]
+
+
+def test_greedy_tokens_take_the_first_maximum():
+    assert oracle.greedy_tokens(np.array([[1.0, 3.0, 3.0, 0.0], [-2.0, -1.0, -1.5, -1.0]])).tolist() == [1, 1]
+
+
+def test_lm_head_logits_match_torch():
+    """Final RMSNorm + LM head equals torch's rms_norm followed by a matmul."""
+    rng = np.random.default_rng(4)
+    h = rng.standard_normal((5, 24))
+    g = rng.uniform(0.5, 1.5, 24)
+    W = rng.standard_normal((24, 40))
+    want = torch.nn.functional.rms_norm(torch.tensor(h), (24,), torch.tensor(g), eps=1e-6) @ torch.tensor(W)
+    np.testing.assert_allclose(oracle.lm_head_logits(h, g, W, 1e-6), want.numpy(), rtol=1e-12, atol=1e-12)
