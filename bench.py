@@ -1,6 +1,6 @@
 """Benchmark of the folded multi-branch verification pass.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 1.5b] [--delta 0.1]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 14b] [--delta 0.1]
 
 One step = one verification pass (every layer: gate, compaction, source
 resolution, QKV, attention, O, FFN, residual) over one denoising block of
@@ -195,11 +195,95 @@ def oracle_sample(cfg, wl, delta, budget_s=12.0):
             break
     per_pass = t_layers / layers * cfg.n_layers
     return {"value": cfg.rows / per_pass, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"float64 oracle on layers 0..{layers - 1} of {cfg.n_layers} of the same workload, "
-                      f"time per layer x {cfg.n_layers}", "passes_per_s": 1.0 / per_pass}
+            "sample": f"float64 oracle on layers 0..{layers - 1} of {cfg.n_layers} of the same workload "
+                      f"(all {cfg.n_requests} requests), time per layer x {cfg.n_layers} (extrapolated)",
+            "passes_per_s": 1.0 / per_pass}
+
+
+def reference_arm(cfg, delta, args, config):
+    """The float64 oracle, as it stands, on the host cores.  A whole pass of a
+    large config takes minutes on the CPU, so every step is a bounded sample of
+    the same workload: layer 0 of one request (requests in turn).  ms_per_step
+    is the measured duration of those steps; value extrapolates them to a whole
+    pass (step time x requests x layers per pass)."""
+    import oracle
+    import synth
+    seed = replica_seed(0)
+    parents = synth.make_trees(cfg, seed)
+    tokens = synth.make_all_tokens(cfg, parents, seed)
+    H = synth.make_hidden(cfg, tokens, seed, "cpu").double().numpy()
+    pk, pv = synth.make_prefix_kv(cfg, seed, "cpu", n_layers=1)
+    pk = pk[0].double().numpy()
+    pv = pv[0].double().numpy()
+    W = oracle.layer_weights_f64(synth.make_layer_weights(cfg, 0, seed, "cpu"))
+    times = []
+    for s in range(args.warmup + args.steps):
+        r = s % cfg.n_requests
+        t0 = time.perf_counter()
+        oracle.folded_layer_resolved(H[r], parents[r], delta, W, pk[r], pv[r], cfg)
+        times.append(time.perf_counter() - t0)
+    t = times[args.warmup:]
+    step_s = sum(t) / len(t)
+    per_pass = step_s * cfg.n_requests * cfg.n_layers
+    v = cfg.rows / per_pass
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"float64 oracle: each step is layer 0 of one request (requests in turn) of the same workload; "
+              f"value = {cfg.rows} rows / (step time x {cfg.n_requests} requests x {cfg.n_layers} layers)")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (random-init N(0,0.02) weights)", "config": config,
+            "passes_per_s": 1.0 / per_pass,
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ per-kernel figures
+
+def family_times(sf, ctx, step_fn, steps):
+    """Per family: (summed ms, launches) over `steps` passes replayed with an
+    event pair around every launch of the family (recorded on the launching
+    stream inside the pass's graph)."""
+    sf.sf_timing_begin(ctx.ctx, sf.FAMILIES)
+    for _ in range(steps):
+        step_fn()
+    t = sf.sf_timing_read(ctx.ctx)
+    sf.sf_timing_begin(ctx.ctx, [])
+    return t
+
+
+def kernel_table(cfg, rc_counts, fam_t, steps, pk):
+    """Per family: time per launch, algorithmic bytes and FLOPs per launch, and
+    the achieved fraction of the bounding roofline (measured peaks)."""
+    work = {}
+    for t_rc in rc_counts:
+        for f, v in layer_work(cfg, int(t_rc)).items():
+            w = work.setdefault(f, {"flops": 0.0, "bytes": 0.0})
+            w["flops"] += v["flops"]
+            w["bytes"] += v["bytes"]
+    out = {}
+    for f, (ms, n) in fam_t.items():
+        if f not in work or n == 0:
+            continue
+        per_pass = n / steps
+        fl, by = work[f]["flops"] / per_pass, work[f]["bytes"] / per_pass
+        t = ms / n / 1e3
+        t_tensor = fl / (pk["bf16_tflops"] * 1e12)
+        t_hbm = by / (pk["hbm_gbs"] * 1e9)
+        out[f] = {"us_per_launch": t * 1e6, "launches_per_pass": per_pass, "bytes": by, "flops": fl,
+                  "gbs": by / t / 1e9, "frac_hbm": by / t / 1e9 / pk["hbm_gbs"],
+                  "tflops": fl / t / 1e12, "frac_tensor": fl / t / 1e12 / pk["bf16_tflops"],
+                  "bound": "tensor" if t_tensor > t_hbm else "hbm"}
+    return out
 
 
 # ------------------------------------------------------------------ config sweep
+
+def rho_quantiles(rho):
+    """Per layer: quantiles (10/50/90 %) of the gate's rho over draft rows."""
+    r = rho[:, :, 1:].reshape(rho.shape[0], -1)
+    return [[float(x) for x in np.quantile(r[l], [0.1, 0.5, 0.9])] for l in range(r.shape[0])]
+
 
 def sweep(args, dev):
     """Folded vs dense throughput for every workload config on this GPU."""
@@ -218,6 +302,7 @@ def sweep(args, dev):
         out = torch.empty_like(wl.hidden)
         fold = torch.empty((nl, cfg.n_requests, cfg.n_branches, cfg.block_len), dtype=torch.uint8, device=dev)
         rcc = torch.empty((nl,), dtype=torch.int32, device=dev)
+        rho = torch.empty(fold.shape, dtype=torch.float32, device=dev)
         pk_ = wl.prefix_k if cfg.prefix_len else None
         pv_ = wl.prefix_v if cfg.prefix_len else None
 
@@ -231,6 +316,7 @@ def sweep(args, dev):
                 ctx.verify(wl.hidden, wl.parents, pk_, pv_, dl, out=out, fold=fold, rc_count=rcc, stream=stream)
             e1.record(stream)
             torch.cuda.synchronize()
+            ctx.sync(stream)
             return e0.elapsed_time(e1) / args.steps
 
         dense_ms = timed(0.0)
@@ -250,10 +336,254 @@ def sweep(args, dev):
                                       pw["bytes"] / (pk["hbm_gbs"] * 1e9) else "hbm",
                     "dense_ms_per_pass": dense_ms, "dense_branch_tokens_per_s": cfg.rows * 1e3 / dense_ms,
                     "dense_pass_roofline_frac": t_roof_d * 1e3 / dense_ms, "speedup_vs_dense": dense_ms / ms}
+            if name == "8b" and cfg.n_drafts:
+                # the gate's rho over draft rows, per layer, from one more pass
+                ctx.set_rho_dump(rho)
+                ctx.verify(wl.hidden, wl.parents, pk_, pv_, dl, out=out, fold=fold, rc_count=rcc, stream=stream)
+                ctx.set_rho_dump(None)
+                ctx.sync(stream)
+                q = rho_quantiles(rho.cpu().numpy())
+                line["rho_q"] = {"quantiles": [0.1, 0.5, 0.9], "per_layer": q}
             print(json.dumps(line), flush=True)
         ctx.close()
         del wl, ctx
         torch.cuda.empty_cache()
+
+
+def gate_sweep(args, dev):
+    """Gate kernel (gate + compaction + resolution + attention RMSNorm) over
+    row counts: the 14B-shaped model's first 3 layers at R = 1, 2, 4, 8
+    requests of main + 8 drafts, delta = 0.1.  L2 is flushed (a 512 MB write)
+    before every pass; inside a pass the FFN weights streamed since the O
+    projection wrote h (about 440 MB) evict it as well.  One JSON line per size:
+    the gate's time per launch at layers 1-2 (their inputs come from the
+    previous layer, as in the pass), algorithmic bytes and GB/s."""
+    import torch
+    import synth
+    import sparse_reuse_gb300 as sf
+    pk = peaks()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for R in (1, 2, 4, 8):
+        cfg = synth.CONFIGS["14b"].with_(n_layers=3, n_requests=R)
+        wl = synth.make_workload(cfg, seed=0, device=dev)
+        ctx = sf.from_config(cfg, wl.weights)
+        stream = torch.cuda.Stream(device=dev)
+        rcc = torch.empty((cfg.n_layers,), dtype=torch.int32, device=dev)
+        for _ in range(args.warmup):
+            ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, 0.1, rc_count=rcc, stream=stream)
+        ctx.sync(stream)
+        sf.sf_timing_begin(ctx.ctx, ["gate"])
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
+            ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, 0.1, rc_count=rcc, stream=stream)
+        ctx.sync(stream)
+        sf.sf_timing_begin(ctx.ctx, [])
+        # the gate's launches of every layer (its launches come in layer
+        # order, the same number per layer), layers 1 and 2 apart from layer 0
+        per = _gate_launch_times(sf, ctx, wl, rcc, stream, flush, args.steps)
+        k = len(per) // cfg.n_layers
+        per_layer = [sum(per[l * k:(l + 1) * k]) for l in range(cfg.n_layers)]
+        rc = rcc.cpu().numpy().tolist()
+        by = [layer_work(cfg, t)["gate"]["bytes"] for t in rc]
+        t_in = sum(per_layer[1:]) / len(per_layer[1:]) / 1e3
+        b_in = sum(by[1:]) / len(by[1:])
+        line = {"gate_sweep": True, "config": workload_desc(cfg), "rows": cfg.rows, "rc_count": rc,
+                "launches_per_layer": k, "us_per_layer_layer0": per_layer[0] * 1e3,
+                "us_per_layer_layers_1_2": t_in * 1e6, "us_per_launch_layers_1_2": [
+                    sum(per[l * k + j] for l in range(1, cfg.n_layers)) / (cfg.n_layers - 1) * 1e3 for j in range(k)],
+                "bytes_per_layer_layers_1_2": b_in, "gbs": b_in / t_in / 1e9,
+                "frac_hbm": b_in / t_in / 1e9 / pk["hbm_gbs"], "peak_gbs": pk["hbm_gbs"],
+                "l2": "flushed before every pass; launches timed one at a time (no overlap between them)"}
+        print(json.dumps(line), flush=True)
+        ctx.close()
+        del wl, ctx
+        torch.cuda.empty_cache()
+
+
+def depth_sweep(args, dev, base):
+    """Drafting-strategy workload: B = 7 one-token drafts as chains of depth
+    D = 1 (seven siblings) .. 4 off the main branch; fold ratio and throughput
+    folded (delta = 0.1) vs dense.  One JSON line per depth."""
+    import torch
+    import synth
+    import sparse_reuse_gb300 as sf
+    for D in synth.DEPTH_SWEEP:
+        cfg = synth.depth_config(base, D)
+        wl = synth.make_workload(cfg, seed=0, device=dev)
+        ctx = sf.from_config(cfg, wl.weights)
+        stream = torch.cuda.Stream(device=dev)
+        nl = cfg.n_layers
+        fold = torch.empty((nl, cfg.n_requests, cfg.n_branches, cfg.block_len), dtype=torch.uint8, device=dev)
+        rcc = torch.empty((nl,), dtype=torch.int32, device=dev)
+        out = torch.empty_like(wl.hidden)
+        res = {}
+        for dl in (0.0, 0.1):
+            for _ in range(args.warmup):
+                ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, dl, out=out, fold=fold, rc_count=rcc,
+                           stream=stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, dl, out=out, fold=fold, rc_count=rcc,
+                           stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ctx.sync(stream)
+            res[dl] = (e0.elapsed_time(e1) / args.steps, fold[:, :, 1:].float().mean().item(),
+                       rcc.float().mean().item())
+        ms, ff, rc = res[0.1]
+        line = {"depth_sweep": True, "config": workload_desc(cfg), "depth": D, "parents": wl.parents[0].tolist(),
+                "delta": 0.1, "fold_ratio": ff, "rc_rows_mean": rc, "ms_per_pass": ms,
+                "branch_tokens_per_s": cfg.rows * 1e3 / ms, "dense_ms_per_pass": res[0.0][0],
+                "dense_branch_tokens_per_s": cfg.rows * 1e3 / res[0.0][0], "speedup_vs_dense": res[0.0][0] / ms}
+        print(json.dumps(line), flush=True)
+        ctx.close()
+        del wl, ctx
+        torch.cuda.empty_cache()
+
+
+def ripple(args, dev, base):
+    """Residual-ripple diagnostic: one child that unmasks one position of a
+    main block with 17 of 32 positions committed.  Prints the gate's rho of
+    the child at every layer and position, and per layer its mean over the
+    committed, still-masked and newly unmasked positions."""
+    import torch
+    import synth
+    import sparse_reuse_gb300 as sf
+    cfg = synth.ripple_config(base)
+    wl = synth.make_workload(cfg, seed=0, device=dev)
+    ctx = sf.from_config(cfg, wl.weights)
+    rho = torch.empty((cfg.n_layers, cfg.n_requests, cfg.n_branches, cfg.block_len), dtype=torch.float32,
+                      device=dev)
+    ctx.set_rho_dump(rho)
+    _, fold, _, _ = ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, cfg.delta)
+    ctx.sync()
+    ctx.set_rho_dump(None)
+    ctx.close()
+    tok = wl.tokens[0]
+    committed = tok[0] != synth.MASK_ID
+    new = (tok[0] == synth.MASK_ID) & (tok[1] != synth.MASK_ID)
+    masked = tok[1] == synth.MASK_ID
+    r = rho[:, 0, 1].cpu().numpy()
+    f = fold[:, 0, 1].cpu().numpy()
+    per_layer = [{"layer": l, "committed": float(r[l, committed].mean()), "masked": float(r[l, masked].mean()),
+                  "new": float(r[l, new].mean()), "folded": int(f[l].sum())} for l in range(cfg.n_layers)]
+    line = {"ripple": True, "config": workload_desc(cfg), "delta": cfg.delta,
+            "positions": {"committed": np.flatnonzero(committed).tolist(), "masked": np.flatnonzero(masked).tolist(),
+                          "new": np.flatnonzero(new).tolist()},
+            "per_layer_mean": per_layer, "rho": [[float(x) for x in row] for row in r]}
+    print(json.dumps(line), flush=True)
+
+
+def head_bench(args, dev, cfg):
+    """Verification head after the pass: final RMSNorm, LM head over the
+    synthetic vocabulary (greedy tokens of every row) and draft acceptance.
+    Times pass + head and the head alone (CUDA events on the stream); the
+    drafts are the workload's own (random tokens), so few match."""
+    import torch
+    import synth
+    import sparse_reuse_gb300 as sf
+    wl = synth.make_workload(cfg, seed=0, device=dev)
+    ctx = sf.from_config(cfg, wl.weights)
+    gain, w_lm = synth.make_head_weights(cfg, synth.HEAD_VOCAB, 0, device=dev)
+    head = sf.Head(d_model=cfg.d_model, vocab=synth.HEAD_VOCAB, dtype=cfg.dtype, max_rows=cfg.rows, final_norm=gain,
+                   w_lm=w_lm, rms_eps=cfg.rms_eps)
+    stream = torch.cuda.Stream(device=dev)
+    out = torch.empty_like(wl.hidden)
+    tok = torch.from_numpy(wl.tokens.astype(np.int32)).to(dev)
+    pred = torch.empty(wl.tokens.shape, dtype=torch.int32, device=dev)
+    acc = torch.empty((cfg.n_requests, cfg.n_branches), dtype=torch.uint8, device=dev)
+    chosen = torch.empty((cfg.n_requests,), dtype=torch.int32, device=dev)
+
+    def run(k, with_pass):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            if with_pass:
+                ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, cfg.delta, out=out, stream=stream,
+                           want_masks=False)
+            head.verify(out, tok, wl.parents, pred=pred, accepted=acc, chosen=chosen, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / k
+
+    run(args.warmup, True)
+    both = run(args.steps, True)
+    alone = run(args.steps, False)
+    ctx.sync(stream)
+    head.close()
+    ctx.close()
+    wb = (2 if cfg.dtype == "bf16" else 4) * cfg.d_model * synth.HEAD_VOCAB
+    line = {"head": True, "config": workload_desc(cfg), "vocab": synth.HEAD_VOCAB, "delta": cfg.delta,
+            "ms_pass_plus_head": both, "ms_head": alone, "head_weight_bytes": wb,
+            "head_gbs": wb / (alone * 1e-3) / 1e9, "head_frac_hbm": wb / (alone * 1e-3) / 1e9 / peaks()["hbm_gbs"],
+            "accepted_drafts": int(acc[:, 1:].sum().item()), "drafts": cfg.n_requests * cfg.n_drafts,
+            "chosen": chosen.cpu().numpy().tolist()}
+    print(json.dumps(line), flush=True)
+
+
+def attention_modes(args, dev, cfg):
+    """Direct attention (every row's block part against its branch's keys)
+    vs the pages' correction (block part for recompute rows, subtract/add
+    correction for folded rows) on the same workload: pass time and the
+    attention kernels' time per pass, CUDA events on the stream."""
+    import torch
+    import synth
+    import sparse_reuse_gb300 as sf
+    wl = synth.make_workload(cfg, seed=0, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    out = torch.empty_like(wl.hidden)
+    res = {}
+    for name, mode in (("direct", sf.SF_ATTN_DIRECT), ("correct", sf.SF_ATTN_CORRECT)):
+        ctx = sf.from_config(cfg, wl.weights)
+        ctx.set_attention_mode(mode)
+
+        def step():
+            ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, cfg.delta, out=out, stream=stream,
+                       want_masks=False)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ctx.sync(stream)
+        fam = family_times(sf, ctx, step, args.steps)
+        ctx.sync(stream)
+        res[name] = {"ms_per_pass": e0.elapsed_time(e1) / args.steps,
+                     "attention_ms_per_pass": {f: fam[f][0] / args.steps for f in ("attn_prefix", "attn_block",
+                                                                                    "attn_correct") if f in fam},
+                     "out": out.float().clone()}
+        ctx.close()
+    diff = (res["correct"]["out"] - res["direct"]["out"]).abs().max().item()
+    scale = res["direct"]["out"].abs().max().item()
+    for r in res.values():
+        r.pop("out")
+    line = {"attention_modes": True, "config": workload_desc(cfg), "delta": cfg.delta, **res,
+            "max_abs_diff_of_outputs": diff, "output_scale": scale}
+    print(json.dumps(line), flush=True)
+
+
+def _gate_launch_times(sf, ctx, wl, rcc, stream, flush, steps):
+    """Mean gate time per layer (ms), from passes timed one at a time."""
+    import torch
+    acc = None
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        sf.sf_timing_begin(ctx.ctx, ["gate"])
+        ctx.verify(wl.hidden, wl.parents, wl.prefix_k, wl.prefix_v, 0.1, rc_count=rcc, stream=stream)
+        t = sf.sf_timing_list(ctx.ctx, "gate")
+        sf.sf_timing_begin(ctx.ctx, [])
+        acc = t if acc is None else [a + b for a, b in zip(acc, t)]
+    ctx.sync(stream)
+    return [a / steps for a in acc]
 
 
 # ------------------------------------------------------------------ main
@@ -264,7 +594,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="1.5b")
+    ap.add_argument("--config", default="14b")
     ap.add_argument("--delta", type=float, default=None)
     ap.add_argument("--drafts", type=int, default=None)
     ap.add_argument("--no-dense", action="store_true")
@@ -275,6 +605,16 @@ def main():
                     help="profiling only: warm-up and timed passes, nothing else, no JSON line")
     ap.add_argument("--sweep", action="store_true",
                     help="every workload config (8B delta sweep, 14B draft sweep): one JSON line each")
+    ap.add_argument("--depth-sweep", action="store_true",
+                    help="drafting strategies: B = 7 one-token drafts in chains of depth 1..4 (the --config model)")
+    ap.add_argument("--ripple", action="store_true",
+                    help="per-layer, per-position rho of a one-token child of a 17/32-committed parent")
+    ap.add_argument("--attention-modes", action="store_true",
+                    help="direct attention vs the pages' subtract/add correction of folded rows (--config model)")
+    ap.add_argument("--head", action="store_true",
+                    help="the verification head (final RMSNorm, LM head, greedy tokens, acceptance) after the pass")
+    ap.add_argument("--gate-sweep", action="store_true",
+                    help="gate kernel GB/s over row counts (14B rows, R = 1..8), L2 flushed between passes")
     args = ap.parse_args()
 
     import torch
@@ -301,23 +641,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        wl = synth.make_workload(cfg, seed=0, device="cpu")
-        times = []
-        samp = None
-        for _ in range(args.warmup + args.steps):
-            samp = oracle_sample(cfg, wl, delta, budget_s=0.0)   # one layer per step
-            times.append(1.0 / samp["passes_per_s"])
-        t = times[args.warmup:]
-        per_pass = sum(t) / len(t)
-        v = cfg.rows / per_pass
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_pass * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": samp["cores"], "kind": "oracle",
-                                 "sample": "float64 oracle, one layer per step, time x n_layers"},
-                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        print(json.dumps(reference_arm(cfg, delta, args, config)))
         return
 
     torch.cuda.set_device(local)
@@ -326,6 +650,21 @@ def main():
 
     if args.sweep:
         sweep(args, dev)
+        return
+    if args.gate_sweep:
+        gate_sweep(args, dev)
+        return
+    if args.depth_sweep:
+        depth_sweep(args, dev, cfg)
+        return
+    if args.ripple:
+        ripple(args, dev, cfg)
+        return
+    if args.head:
+        head_bench(args, dev, cfg)
+        return
+    if args.attention_modes:
+        attention_modes(args, dev, cfg)
         return
 
     wl = synth.make_workload(cfg, seed=replica_seed(rank), device=dev)
@@ -351,7 +690,7 @@ def main():
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        s0 = stats0 = ctx.stats()["kernel_launches"]
+        s0 = ctx.stats()["kernel_launches"]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(k):
@@ -359,6 +698,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
+        ctx.sync(stream)   # a device-side check that fired (e.g. a bounded wait that gave up) fails the run
         ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
         return ms, ctx.stats()["kernel_launches"] - s0
 
@@ -380,39 +720,25 @@ def main():
                  "ms_per_step": dms / args.steps, "passes_per_s": world * args.steps / (dms / 1e3),
                  "rc_count": rcc.cpu().numpy().tolist()}
 
-    # per-family kernel timing (direct launches bracketed by events on the same stream)
-    sf.sf_timing_begin(ctx.ctx, sf.FAMILIES)
-    for _ in range(args.steps):
-        step(delta)
-    fam_t = sf.sf_timing_read(ctx.ctx)
-    sf.sf_timing_begin(ctx.ctx, [])
+    # per-family kernel timing (the pass replayed with an event pair around
+    # every launch of a family, on the launching stream)
     pk = peaks()
-    work = {}
-    for t_rc in rc_fold:
-        for f, v in layer_work(cfg, int(t_rc)).items():
-            w = work.setdefault(f, {"flops": 0.0, "bytes": 0.0})
-            w["flops"] += v["flops"]
-            w["bytes"] += v["bytes"]
+    fam_t = family_times(sf, ctx, lambda: step(delta), args.steps)
+    ctx.sync(stream)
+    kernels = kernel_table(cfg, rc_fold, fam_t, args.steps, pk)
     total_fam_ms = sum(v[0] for v in fam_t.values())
-    dom = max((f for f in fam_t if f in work), key=lambda f: fam_t[f][0])
-    dom_ms, dom_n = fam_t[dom]
-    per_launch_s = dom_ms / dom_n / 1e3
-    launches_per_pass = dom_n / args.steps
-    flops_l = work[dom]["flops"] / launches_per_pass
-    bytes_l = work[dom]["bytes"] / launches_per_pass
-    t_tensor = flops_l / (pk["bf16_tflops"] * 1e12)
-    t_hbm = bytes_l / (pk["hbm_gbs"] * 1e9)
-    if t_tensor > t_hbm:
-        roof = {"bound": "tensor", "achieved": flops_l / per_launch_s / 1e12, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s"}
+    dom = max((f for f in fam_t if f in kernels), key=lambda f: fam_t[f][0])
+    kd = kernels[dom]
+    if kd["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
     else:
-        roof = {"bound": "hbm", "achieved": bytes_l / per_launch_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": kd["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = NCU_TRAFFIC.get((cfg.name, dom))
     roof["traffic_unit"] = "bytes per launch"
     roof["kernel"] = dom
     roof["peak_source"] = pk["source"]
-    roof["share_of_pass"] = dom_ms / total_fam_ms if total_fam_ms else None
+    roof["share_of_pass"] = fam_t[dom][0] / total_fam_ms if total_fam_ms else None
     pw = pass_work(cfg, rc_fold)
     t_roof = max(pw["flops"] / (pk["bf16_tflops"] * 1e12), pw["bytes"] / (pk["hbm_gbs"] * 1e9))
 
@@ -442,6 +768,7 @@ def main():
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
     barrier()
+    ctx.sync(stream)
     e2e_s = max_over_ranks(e2e_s, dist, dev)
     e2e = {"value": whole_job_rate(world, T, args.steps, e2e_s), "unit": UNIT,
            "h2d_bytes_per_step": h_host.numel() * h_host.element_size(),
@@ -456,7 +783,9 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (random-init N(0,0.02) weights)",
-                "config": dict(config, l2="weights streamed per pass %.2f GB > 129 MB L2" % (weight_bytes(cfg) / 1e9)),
+                "config": config,
+                "l2": "no flush: the weights streamed per pass (%.2f GB) exceed the 129 MB L2"
+                      % (weight_bytes(cfg) / 1e9),
                 "passes_per_s": world * args.steps / (ms / 1e3),
                 "fold_fraction": fold_frac, "rc_count_per_layer": rc_fold,
                 "dense": dense,
@@ -464,8 +793,9 @@ def main():
                 "pass_roofline": {"t_roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
                                   "flops": pw["flops"], "bytes": pw["bytes"]},
                 "roofline": roof,
-                "kernel_ms_per_pass": {f: v[0] / args.steps for f, v in fam_t.items()},
+                "kernels": kernels,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "device_checks": "clean",
                 "clocks": clk.summary()}
         print(json.dumps(line))
     ctx.close()

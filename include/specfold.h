@@ -134,6 +134,36 @@ sf_status sf_verify(sf_ctx* ctx, void* stream, const void* hidden_in, const int3
  * (SF_ERR_INVALID_ARG otherwise). */
 sf_status sf_set_debug(sf_ctx* ctx, float* layer_hidden, int32_t* rc_rows);
 
+/* Gate diagnostic for later sf_verify calls (NULL turns it off): the relative
+ * residual rho = ||H_i[n] - H_par(i)[n]|| / ||H_par(i)[n]|| of every row at
+ * every layer, as the gate computed it in fp32 ([KR] "What is different";
+ * [SF] §3.1, and the per-layer, per-position residual ripple of [SF] §4.4,
+ * Figure 6).  The main branch has no parent: its rows get NaN.  A zero parent
+ * row gives 0 when the child row is zero too, else +inf.
+ *   rho  device fp32 [n_layers, R, B+1, L], 4-byte aligned (SF_ERR_INVALID_ARG
+ *        otherwise).
+ * The fold decision itself is taken as ||diff||^2 <= delta^2 ||parent||^2 and
+ * does not go through this value. */
+sf_status sf_set_rho_dump(sf_ctx* ctx, float* rho);
+
+/* How a folded row's attention is computed (both give the branch's exact
+ * attention; [SF] §A.1):
+ *   SF_ATTN_DIRECT   every row attends to the shared prefix (through its
+ *                    source query's prefix partial) and to its branch's own L
+ *                    block keys (default);
+ *   SF_ATTN_CORRECT  only recompute rows run the block attention, keeping
+ *                    their merged softmax state (max, denominator, weighted
+ *                    value sum); a folded row starts from its source row's
+ *                    state, removes the source branch's contributions at the
+ *                    block positions where its own branch's keys differ and
+ *                    adds its own there (the subtract/add correction of
+ *                    [SF] §A.1, App. B, applied against the nearest
+ *                    recomputed ancestor as in §A.3).
+ * Applies to later sf_verify calls.  Errors: SF_ERR_INVALID_ARG (null ctx or
+ * unknown mode). */
+typedef enum sf_attn_mode { SF_ATTN_DIRECT = 0, SF_ATTN_CORRECT = 1 } sf_attn_mode;
+sf_status sf_set_attention_mode(sf_ctx* ctx, int mode);
+
 /* Wait for the context's work on `stream` to finish and report a device-side
  * check that fired (SF_ERR_DEVICE_ASSERT) or a CUDA error.  A device-side
  * check word is reported once: it is cleared on return, so a caller that
@@ -142,10 +172,11 @@ sf_status sf_set_debug(sf_ctx* ctx, float* layer_hidden, int32_t* rc_rows);
 sf_status sf_sync_status(sf_ctx* ctx, void* stream);
 
 /* Failure injection for tests of the detection path (no counterpart in the
- * method): while `on` is nonzero, later sf_verify passes never signal the
- * completion of layer 0's compaction.  The recompute rows' bounded waits for
- * it give up after about 2 s and raise the timeout bit of the device check
- * word; the pass finishes with wrong values and sf_sync_status reports
+ * method): while `on` is nonzero, the first row of layer 0 in later sf_verify
+ * passes never reports its gate decision to the other rows.  Their bounded
+ * waits for it (the compaction's prefix look-back and source resolution) give
+ * up after about 2 s and raise the timeout bit of the device check word; the
+ * pass finishes with wrong values and sf_sync_status reports
  * SF_ERR_DEVICE_ASSERT.  No GPU fault, trap or hang is involved.
  * Errors: SF_ERR_INVALID_ARG (null ctx). */
 sf_status sf_inject_stall(sf_ctx* ctx, int on);
@@ -173,7 +204,8 @@ typedef enum sf_kernel_family {
   SF_K_GEMM_DOWN = 7,   /* down projection */
   SF_K_RESIDUAL = 8,    /* last layer's residual + output cast */
   SF_K_AUX = 9,         /* anything else (GEMM epilogue passes) */
-  SF_K_COUNT = 10
+  SF_K_ATTN_CORRECT = 10, /* attention correction of the folded rows (SF_ATTN_CORRECT) */
+  SF_K_COUNT = 11
 } sf_kernel_family;
 
 typedef struct sf_stats {
@@ -199,6 +231,14 @@ sf_status sf_set_graphs(sf_ctx* ctx, int use_graphs);
  * last sf_timing_begin.  total_ms and launches have SF_K_COUNT entries. */
 sf_status sf_timing_begin(sf_ctx* ctx, unsigned family_mask);
 sf_status sf_timing_read(sf_ctx* ctx, double* total_ms, int64_t* launches);
+
+/* The same events one launch at a time: the durations (ms) of the timed
+ * launches of `family` since the last sf_timing_begin, in launch order (a
+ * pass launches the gate once per layer, so its list is per layer).  Writes at
+ * most max_n entries to ms and the number of timed launches of the family to
+ * *n (which may exceed max_n).  Errors: SF_ERR_INVALID_ARG (null pointer,
+ * family outside 0..SF_K_COUNT-1, max_n < 0), SF_ERR_CUDA. */
+sf_status sf_timing_list(sf_ctx* ctx, int family, double* ms, int max_n, int* n);
 
 #ifdef __cplusplus
 }

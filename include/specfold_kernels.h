@@ -70,8 +70,15 @@ sf_status sfk_gemm_bf16(void* stream, const void* X, int rows_cap, const void* W
  * a misaligned pointer), SF_ERR_SHAPE, SF_ERR_TREE; SF_ERR_CUDA if the set-up
  * or launch fails.
  *
+ * Device-side checks: the kernel's index checks cannot fire for a tree that
+ * passed the host checks; if one does, *rc_count is set to -1 (the kernel has
+ * no other error output), so a caller that reads the count sees it.
+ *
  * The first call on a device (with that device current) looks up the
- * array's device address; make that first call before any stream capture.
+ * array's device address and caches it for the life of the process; make that
+ * first call before any stream capture.  The cached address does not survive
+ * cudaDeviceReset or any other teardown of the device's primary context:
+ * after one, the library has to be unloaded and loaded again.
  * Every call on a device shares the one array, and the call clears the parts
  * that must start at zero: calls that overlap on the GPU (different streams,
  * or host threads without ordering) race on it and must be serialised by the

@@ -22,13 +22,15 @@ SF_OK, SF_ERR_INVALID_ARG, SF_ERR_SHAPE, SF_ERR_TREE, SF_ERR_UNSUPPORTED, SF_ERR
     SF_ERR_DEVICE_ASSERT = range(8)
 SF_F32, SF_BF16 = 0, 1
 FAMILIES = ["gate", "norm", "gemm_qkv", "attn_prefix", "attn_block", "gemm_o", "gemm_gateup", "gemm_down",
-            "residual", "aux"]
+            "residual", "aux", "attn_correct"]
+SF_ATTN_DIRECT, SF_ATTN_CORRECT = 0, 1
 SF_K_COUNT = len(FAMILIES)
 
 # every symbol include/specfold.h declares
-EXPORTS = ["sf_create", "sf_verify", "sf_set_debug", "sf_sync_status", "sf_destroy", "sf_status_str",
-           "sf_last_error", "sf_get_stats", "sf_set_graphs", "sf_timing_begin", "sf_timing_read",
-           "sfk_gemm_bf16", "sfk_gate_noalloc", "sf_inject_stall"]
+EXPORTS = ["sf_create", "sf_verify", "sf_set_debug", "sf_set_rho_dump", "sf_set_attention_mode", "sf_sync_status", "sf_destroy", "sf_status_str",
+           "sf_last_error", "sf_get_stats", "sf_set_graphs", "sf_timing_begin", "sf_timing_read", "sf_timing_list",
+           "sfk_gemm_bf16", "sfk_gate_noalloc", "sf_inject_stall",
+           "sf_head_create", "sf_head_verify", "sf_head_last_error", "sf_head_destroy"]
 
 
 class SfShapes(ctypes.Structure):
@@ -42,6 +44,11 @@ class SfShapes(ctypes.Structure):
 class SfLayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")]
+
+
+class SfHeadShapes(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("vocab", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("rms_eps", ctypes.c_float), ("max_rows", ctypes.c_int)]
 
 
 class SfStats(ctypes.Structure):
@@ -63,6 +70,8 @@ def _load() -> ctypes.CDLL:
     lib.sf_create.argtypes = [ctypes.POINTER(SfShapes), ctypes.POINTER(SfLayerWeights), ctypes.POINTER(vp)]
     lib.sf_verify.argtypes = [vp, vp, vp, i32p, vp, vp, c_int, c_int, c_int, c_float, vp, vp, vp, vp]
     lib.sf_set_debug.argtypes = [vp, vp, vp]
+    lib.sf_set_rho_dump.argtypes = [vp, vp]
+    lib.sf_set_attention_mode.argtypes = [vp, c_int]
     lib.sf_sync_status.argtypes = [vp, vp]
     lib.sf_inject_stall.argtypes = [vp, c_int]
     lib.sf_destroy.argtypes = [vp]
@@ -74,12 +83,18 @@ def _load() -> ctypes.CDLL:
     lib.sf_set_graphs.argtypes = [vp, c_int]
     lib.sf_timing_begin.argtypes = [vp, ctypes.c_uint]
     lib.sf_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+    lib.sf_timing_list.argtypes = [vp, c_int, ctypes.POINTER(ctypes.c_double), c_int, ctypes.POINTER(c_int)]
     lib.sfk_gemm_bf16.argtypes = [vp, vp, c_int, vp, c_int, c_int, vp, c_int, vp, c_int, c_int, vp]
     lib.sfk_gate_noalloc.argtypes = [vp, vp, c_int, i32p, c_int, c_int, c_int, c_int, c_float, vp, vp, vp, vp, vp,
                                      vp]
+    lib.sf_head_create.argtypes = [ctypes.POINTER(SfHeadShapes), vp, vp, ctypes.POINTER(vp)]
+    lib.sf_head_verify.argtypes = [vp, vp, vp, vp, i32p, c_int, c_int, c_int, vp, vp, vp]
+    lib.sf_head_last_error.argtypes = [vp]
+    lib.sf_head_last_error.restype = ctypes.c_char_p
+    lib.sf_head_destroy.argtypes = [vp]
     for name in EXPORTS:
         fn = getattr(lib, name)
-        if name not in ("sf_status_str", "sf_last_error"):
+        if name not in ("sf_status_str", "sf_last_error", "sf_head_last_error"):
             fn.restype = c_int
     return lib
 
@@ -100,11 +115,11 @@ class _LazyLib:
 lib = _LazyLib()
 
 
-def _check(st: int, ctx=None, what: str = ""):
+def _check(st: int, ctx=None, what: str = "", head=None):
     if st != SF_OK:
         msg = lib.sf_status_str(st).decode()
-        if ctx:
-            extra = lib.sf_last_error(ctx).decode()
+        if ctx or head:
+            extra = (lib.sf_last_error(ctx) if ctx else lib.sf_head_last_error(head)).decode()
             if extra:
                 msg += f": {extra}"
         raise SpecFoldError(st, f"{what}: {msg}" if what else msg)
@@ -141,6 +156,14 @@ def sf_verify(ctx, stream, hidden_in, parent, prefix_k, prefix_v, R, B, P, delta
 
 def sf_set_debug(ctx, layer_hidden, rc_rows) -> None:
     _check(lib.sf_set_debug(ctx, layer_hidden, rc_rows), ctx, "sf_set_debug")
+
+
+def sf_set_attention_mode(ctx, mode: int) -> None:
+    _check(lib.sf_set_attention_mode(ctx, int(mode)), ctx, "sf_set_attention_mode")
+
+
+def sf_set_rho_dump(ctx, rho) -> None:
+    _check(lib.sf_set_rho_dump(ctx, rho), ctx, "sf_set_rho_dump")
 
 
 def sf_sync_status(ctx, stream) -> None:
@@ -180,6 +203,15 @@ def sf_timing_read(ctx) -> dict:
     return {FAMILIES[i]: (ms[i], n[i]) for i in range(SF_K_COUNT) if n[i] > 0}
 
 
+def sf_timing_list(ctx, family: str) -> List[float]:
+    """Durations (ms) of the timed launches of one family, in launch order."""
+    n = ctypes.c_int(0)
+    _check(lib.sf_timing_list(ctx, FAMILIES.index(family), None, 0, ctypes.byref(n)), ctx, "sf_timing_list")
+    buf = (ctypes.c_double * max(1, n.value))()
+    _check(lib.sf_timing_list(ctx, FAMILIES.index(family), buf, n.value, ctypes.byref(n)), ctx, "sf_timing_list")
+    return [buf[i] for i in range(n.value)]
+
+
 def sfk_gemm_bf16(stream, X, rows_cap, W, M, K, count, dense_count, Y, ldy, splits, err=None) -> None:
     _check(lib.sfk_gemm_bf16(stream, X, int(rows_cap), W, int(M), int(K), count, int(dense_count), Y, int(ldy),
                              int(splits), err), None, "sfk_gemm_bf16")
@@ -191,6 +223,22 @@ def sfk_gate_noalloc(stream, hidden, dtype, parent, R, B, L, d, delta, H_out, fo
     _check(lib.sfk_gate_noalloc(stream, hidden, int(dtype), par.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                 int(R), int(B), int(L), int(d), float(delta), H_out, fold, rc, rcslot, src,
                                 rc_count), None, "sfk_gate_noalloc")
+
+
+def sf_head_create(shapes: SfHeadShapes, final_norm, w_lm) -> int:
+    h = ctypes.c_void_p()
+    _check(lib.sf_head_create(ctypes.byref(shapes), final_norm, w_lm, ctypes.byref(h)), None, "sf_head_create")
+    return h.value
+
+
+def sf_head_verify(head, stream, hidden, tokens, parent, R, B, L, pred, accepted=None, chosen=None) -> None:
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    _check(lib.sf_head_verify(head, stream, hidden, tokens, par.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                              int(R), int(B), int(L), pred, accepted, chosen), None, "sf_head_verify", head=head)
+
+
+def sf_head_destroy(head) -> None:
+    _check(lib.sf_head_destroy(head), None, "sf_head_destroy")
 
 
 # ---------------------------------------------------------------- torch convenience
@@ -253,6 +301,12 @@ class SpecFold:
     def set_debug(self, layer_hidden=None, rc_rows=None):
         sf_set_debug(self.ctx, _ptr(layer_hidden), _ptr(rc_rows))
 
+    def set_attention_mode(self, mode: int):
+        sf_set_attention_mode(self.ctx, mode)
+
+    def set_rho_dump(self, rho=None):
+        sf_set_rho_dump(self.ctx, _ptr(rho))
+
     def sync(self, stream=None):
         sf_sync_status(self.ctx, _stream_handle(stream))
 
@@ -261,6 +315,50 @@ class SpecFold:
 
     def set_graphs(self, on: bool):
         sf_set_graphs(self.ctx, on)
+
+
+class Head:
+    """The verification head over torch tensors: final RMSNorm, LM head,
+    greedy tokens and draft acceptance of a pass output.
+
+    final_norm: fp32 CUDA tensor [d]; w_lm: CUDA tensor [d, vocab] in the
+    context dtype."""
+
+    def __init__(self, *, d_model, vocab, dtype, max_rows, final_norm, w_lm, rms_eps=1e-6):
+        for name, t in (("final_norm", final_norm), ("w_lm", w_lm)):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        self.shapes = SfHeadShapes(d_model, vocab, SF_BF16 if dtype in ("bf16", SF_BF16) else SF_F32, rms_eps,
+                                   max_rows)
+        self.head = sf_head_create(self.shapes, _ptr(final_norm), _ptr(w_lm))
+
+    def close(self):
+        if getattr(self, "head", None):
+            sf_head_destroy(self.head)
+            self.head = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def verify(self, hidden, tokens, parent, *, pred=None, accepted=None, chosen=None, stream=None):
+        """Enqueue the head for one pass output; returns (pred, accepted, chosen)."""
+        import torch
+        parent = np.asarray(parent, dtype=np.int32)
+        R, Bp = parent.shape
+        L = int(hidden.shape[2])
+        dev = hidden.device
+        if pred is None:
+            pred = torch.empty((R, Bp, L), dtype=torch.int32, device=dev)
+        if accepted is None:
+            accepted = torch.empty((R, Bp), dtype=torch.uint8, device=dev)
+        if chosen is None:
+            chosen = torch.empty((R,), dtype=torch.int32, device=dev)
+        sf_head_verify(self.head, _stream_handle(stream), _ptr(hidden), _ptr(tokens), parent, R, Bp - 1, L,
+                       _ptr(pred), _ptr(accepted), _ptr(chosen))
+        return pred, accepted, chosen
 
 
 def from_config(cfg, weights, max_requests=None, max_branches=None, max_prefix=None) -> SpecFold:

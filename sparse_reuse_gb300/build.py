@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecfold.so")
 
-SOURCES = ["sf_api.cu", "sf_gate.cu", "sf_gemm.cu", "sf_gemm_tc.cu", "sf_attn.cu"]
+SOURCES = ["sf_api.cu", "sf_gate.cu", "sf_gemm.cu", "sf_gemm_tc.cu", "sf_attn.cu", "sf_head.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                 "-I", INCLUDE, "-I", CSRC]

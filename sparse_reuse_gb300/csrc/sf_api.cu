@@ -61,7 +61,8 @@ void free_ctx(sf_ctx* c) {
     cudaFree(L.wqkv); cudaFree(L.wo); cudaFree(L.wgu); cudaFree(L.wd); cudaFree(L.g1); cudaFree(L.g2);
   }
   void* bufs[] = {c->H, c->h, c->fphys, c->xn, c->qkv, c->attn, c->u, c->y32, c->part_o, c->part_ml,
-                  c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->epoch,
+                  c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->epoch, c->scan,
+                  c->gate_ss,
                   c->err_dev, c->rope};
   for (void* b : bufs) cudaFree(b);
   if (c->err_host) cudaFreeHost(c->err_host);
@@ -183,7 +184,9 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     ga.xn = c->xn;
     ga.gain = W.g1;
     ga.eps = s.rms_eps;
-    ga.done = c->epoch + 1;
+    ga.scan = c->scan;
+    ga.row_ss = c->gate_ss;
+    ga.rho_user = c->dbg_rho ? c->dbg_rho + (size_t)l * T : nullptr;
     ga.stall = c->inject_stall && l == 0;
     ga.epoch = c->epoch;
     ga.layer = l;
@@ -206,6 +209,8 @@ cudaError_t enqueue_pass(sf_ctx* c, Launch& lc, const PassArgs& p) {
     a.R = p.R; a.Bp = Bp; a.L = L; a.P = p.P; a.T = T;
     a.nq = s.n_q_heads; a.nkv = s.n_kv_heads; a.hd = s.head_dim;
     a.target_ctas = c->sm_count;
+    a.mode = c->attn_mode;
+    a.rc = c->rc;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
     a.err = c->err_dev;
     if (launch_attention(lc, bf16, a) != cudaSuccess) return lc.err;
@@ -334,6 +339,8 @@ sf_status sf_create(const sf_shapes* shapes, const sf_layer_weights* layers, sf_
   SF_TRY(dalloc(&c->meta, (size_t)(s.max_requests + 2) * 4));
   SF_TRY(dalloc(&c->ticket, 64));
   SF_TRY(dalloc(&c->epoch, 64));
+  SF_TRY(dalloc(&c->scan, (size_t)T * 8));
+  SF_TRY(dalloc(&c->gate_ss, (size_t)T * 4));
   SF_TRY(dalloc(&c->err_dev, 64));
   SF_TRY(cudaHostAlloc((void**)&c->err_host, 64, cudaHostAllocDefault));
   *c->err_host = 0;
@@ -417,7 +424,8 @@ sf_status sf_verify(sf_ctx* c, void* stream, const void* hidden_in, const int32_
     key.hidden_in = hidden_in; key.prefix_k = prefix_k; key.prefix_v = prefix_v; key.hidden_out = hidden_out;
     key.fold = fold_mask; key.src = src; key.rc_count = rc_count; key.dbg_hidden = c->dbg_hidden;
     key.stall = c->inject_stall;
-    key.dbg_rc = c->dbg_rc; key.stream = stream; key.R = R; key.B = B; key.P = P; key.delta = delta;
+    key.attn_mode = c->attn_mode;
+    key.dbg_rc = c->dbg_rc; key.dbg_rho = c->dbg_rho; key.stream = stream; key.R = R; key.B = B; key.P = P; key.delta = delta;
     key.parent.assign(parent, parent + R * Bp);
     if (!(c->graph_valid && key == c->graph_key)) {
       c->graph_valid = false;
@@ -498,6 +506,19 @@ sf_status sf_set_debug(sf_ctx* c, float* layer_hidden, int32_t* rc_rows) {
   return SF_OK;
 }
 
+sf_status sf_set_attention_mode(sf_ctx* c, int mode) {
+  if (!c || (mode != SF_ATTN_DIRECT && mode != SF_ATTN_CORRECT)) return SF_ERR_INVALID_ARG;
+  c->attn_mode = mode;
+  return SF_OK;
+}
+
+sf_status sf_set_rho_dump(sf_ctx* c, float* rho) {
+  if (!c) return SF_ERR_INVALID_ARG;
+  if (misaligned(rho, 4)) return fail(c, SF_ERR_INVALID_ARG, "rho needs 4-byte alignment");
+  c->dbg_rho = rho;
+  return SF_OK;
+}
+
 sf_status sf_sync_status(sf_ctx* c, void* stream) {
   if (!c) return SF_ERR_INVALID_ARG;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
@@ -567,6 +588,22 @@ sf_status sf_timing_read(sf_ctx* c, double* total_ms, int64_t* launches) {
     total_ms[c->ev_family[i]] += ms;
     launches[c->ev_family[i]] += 1;
   }
+  return SF_OK;
+}
+
+sf_status sf_timing_list(sf_ctx* c, int family, double* ms, int max_n, int* n) {
+  if (!c || !n || max_n < 0 || (max_n > 0 && !ms) || family < 0 || family >= SF_K_COUNT) return SF_ERR_INVALID_ARG;
+  int k = 0;
+  for (size_t i = 0; i < c->ev_used; ++i) {
+    if (c->ev_family[i] != family) continue;
+    cudaError_t e = cudaEventSynchronize(c->ev_stop[i]);
+    if (e != cudaSuccess) return fail(c, SF_ERR_CUDA, "event sync: %s", cudaGetErrorString(e));
+    float t = 0.f;
+    cudaEventElapsedTime(&t, c->ev_start[i], c->ev_stop[i]);
+    if (k < max_n) ms[k] = t;
+    ++k;
+  }
+  *n = k;
   return SF_OK;
 }
 

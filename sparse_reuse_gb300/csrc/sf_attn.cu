@@ -471,9 +471,8 @@ constexpr int kTcStages = 4;
 constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per row group)
 constexpr int kTcMinKeysPerSplit = 512;
 constexpr int kTcMaxSplits = 4;
-// Prefixes of at least this many keys take the tcgen05 kernel; shorter ones
-// the mma.sync kernel, whose smaller fixed cost per CTA wins there.
-constexpr int kTcMinPrefix = 2048;
+// Prefixes of at least this many keys take the tcgen05 kernel.
+constexpr int kTcMinPrefix = 1;
 constexpr float kTcRescaleLog2 = 8.f;
 
 // Few long splits: the fixed cost of a CTA (TMEM, barriers, the first scores,
@@ -490,7 +489,9 @@ __host__ __device__ __forceinline__ Splits tc_split_len(int P, int S) {
 
 inline Splits tc_splits(int P, int groups, int target_ctas) {
   int S = target_ctas / (2 * (groups > 0 ? groups : 1));
-  const int by_len = P / kTcMinKeysPerSplit;
+  // long prefixes: at least 512 keys a split; short ones (a latency-bound
+  // job with few query tiles) split down to two 64-key blocks
+  const int by_len = P / (P >= 2048 ? kTcMinKeysPerSplit : 2 * kKB);
   S = S > by_len ? by_len : S;
   S = S < 1 ? 1 : (S > kTcMaxSplits ? kTcMaxSplits : S);
   return tc_split_len(P, S);
@@ -986,6 +987,247 @@ __global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
   }
 }
 
+// ------------------------------------------------------------ tcgen05 block path
+//
+// Block attention + merge on the 5th-generation tensor cores: CTA = 128 query
+// vectors of one branch and KV head (one per TMEM lane and thread), query
+// vector v = block position v / G with query head kvh * G + v % G, its query
+// the one of the row's resolved source.  Keys and values are the branch's own
+// block table K_i[m] = QKV[rcslot(i, m)], gathered with asynchronous copies
+// into 128-byte-swizzled tiles of NK = 32 or 64 keys (zero past L):
+//   S = Q K^T   one tcgen05.mma chain (K-major Q and K), S in TMEM;
+//   P = exp2(S - m_b) per row by its thread, bf16 into swizzled shared memory;
+//   O = P V     tcgen05.mma (V MN-major), O in the same TMEM columns as S,
+//               which every thread has read by then;
+// then each thread merges its row with the query's prefix partial state by
+// log-sum-exp and writes the normalised bf16 output.
+constexpr int kBlkQ = 128;
+constexpr int kBlkMaxKeys = 64;
+
+// Shared memory: Q (128 rows x HD, as 64-dim halves), then the K and V tiles
+// of NK keys (per 64-dim half NK rows of 128 bytes), then two mbarriers and
+// the TMEM address.  P (128 rows x NK keys, bf16) reuses Q's space once
+// S = Q K^T has completed.
+template <int HD>
+struct BlkLayout {
+  static constexpr int QH = HD / 64;
+  static constexpr int Q_HALF = kBlkQ * 128;  // 128 rows x 64 dims
+  static constexpr int TMEM_COLS = HD;        // S in columns [0, NK), then O in [0, HD)
+  static __host__ __device__ constexpr int kv_half(int nk) { return nk * 128; }
+  static __host__ __device__ constexpr int off_k() { return QH * Q_HALF; }
+  static __host__ __device__ constexpr int off_v(int nk) { return off_k() + QH * kv_half(nk); }
+  static __host__ __device__ constexpr int off_bar(int nk) { return off_v(nk) + QH * kv_half(nk); }
+  static __host__ __device__ constexpr int bytes(int nk) { return off_bar(nk) + 64 + 1024; }
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kBlkQ) attn_block_tc(const AttnArgs a) {
+  using Lay = BlkLayout<HD>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int NK = a.L <= 32 ? 32 : 64;
+  const int KVH = Lay::kv_half(NK);
+  unsigned char* sQ = base;
+  unsigned char* sK = base + Lay::off_k();
+  unsigned char* sV = base + Lay::off_v(NK);
+  unsigned char* sP = base;  // over Q once S = Q K^T has completed
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + Lay::off_bar(NK));  // [0] S done, [1] O done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+  __shared__ int slot[kBlkMaxKeys];
+  __shared__ int pos[kBlkMaxKeys];  // block positions of this CTA's query rows
+  __shared__ int s_npos;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int rb = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;  // rb = r * Bp + i
+  const int G = a.nq / a.nkv, L = a.L;
+  const int q0 = blockIdx.x * kBlkQ;
+  const bool correct = a.mode == SF_ATTN_CORRECT;
+  // Every kernel of the pass lets its dependants start only after its own
+  // dependency wait, so the kernels before the previous one have completed
+  // when this grid starts: with a prefix kernel in between, the source slots
+  // and the recompute list (gate kernel) and the projected rows are read
+  // before the wait, past L1.
+  if (a.P == 0) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  const int cnt = __ldcg(a.meta);
+  for (int m = tid; m < kBlkMaxKeys; m += kBlkQ) {
+    int g = m < L ? __ldcg(a.rcslot + rb * L + m) : 0;
+    if (g < 0 || g >= cnt) {
+      raise_error(a.err, kErrAttn);
+      g = 0;
+    }
+    slot[m] = g;
+  }
+  __syncthreads();
+  // the rows of the branch this kernel answers for: all of them, or with the
+  // correction mode only the rows that recompute (their own source)
+  if (tid == 0) {
+    int np = 0;
+    for (int m = 0; m < L; ++m)
+      if (!correct || __ldcg(a.rc + slot[m]) == rb * L + m) pos[np++] = m;
+    s_npos = np;
+  }
+  __syncthreads();
+  const int nqv = s_npos * G;
+  if (q0 >= nqv) return;  // uniform over the CTA
+  const int v = q0 + tid;
+  const bool live = v < nqv;
+  const int vn = live ? pos[v / G] : 0;  // block position of this thread's query row
+  if (tid == 0) {
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tmem_slot, Lay::TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  // gather: this thread's query row, and keys/values m = tid / 2 (two threads
+  // per key, one per 64-dim half when HD = 128)
+  const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
+  {
+    const bf16* src = qkv + (size_t)slot[vn] * a.ld_qkv + (kvh * G + (live ? v % G : 0)) * HD;
+#pragma unroll
+    for (int c = 0; c < HD / 8; ++c)
+      cp_async16(sQ + (c >> 3) * Lay::Q_HALF + tid * 128 + (((c & 7) ^ (tid & 7)) << 4), src + c * 8, live);
+    const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
+    for (int idx = tid; idx < NK * (HD / 8); idx += kBlkQ) {
+      const int m = idx / (HD / 8), c = idx % (HD / 8);
+      const bf16* row = qkv + (size_t)slot[m] * a.ld_qkv;
+      const int off = (c >> 3) * KVH + m * 128 + (((c & 7) ^ (m & 7)) << 4);
+      cp_async16(sK + off, row + koff + c * 8, m < L);
+      cp_async16(sV + off, row + voff + c * 8, m < L);
+    }
+    cp_async_commit();
+  }
+  if (a.P > 0) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  // the prefix state of this thread's query (previous kernel)
+  size_t qi = 0;
+  float mp = 0.f, lp = 0.f;
+  if (live) qi = (size_t)slot[vn] * a.nq + kvh * G + v % G;
+  if (a.P > 0 && live) {
+    mp = a.part_ml[qi * 2];
+    lp = a.part_ml[qi * 2 + 1];
+  }
+  cp_async_wait<0>();
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0) {
+    const uint32_t idesc = tc::idesc_bf16_f32(kBlkQ, NK);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const uint64_t dq = tc::sw128_kmajor_desc(smem_addr(sQ + (kk >> 2) * Lay::Q_HALF + (kk & 3) * 32));
+      const uint64_t dk = tc::sw128_kmajor_desc(smem_addr(sK + (kk >> 2) * KVH + (kk & 3) * 32));
+      tc::mma_bf16(tmem, dq, dk, idesc, kk > 0 ? 1u : 0u);
+    }
+    tc::mma_commit(&bar[0]);
+  }
+  const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+  tc::mbar_wait(&bar[0], 0, a.err);
+  tc::fence_after_sync();
+  // softmax of the row over its L block keys (log2 units)
+  float sc[kBlkMaxKeys];
+  tc::tmem_ld32(tl, *reinterpret_cast<float(*)[32]>(sc));
+  if (NK > 32) tc::tmem_ld32(tl + 32, *reinterpret_cast<float(*)[32]>(sc + 32));
+  float mb = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kBlkMaxKeys; ++k) {
+    if (k < NK) {
+      sc[k] = k < L ? sc[k] * a.scale_log2 : -INFINITY;
+      mb = fmaxf(mb, sc[k]);
+    }
+  }
+  float lb = 0.f;
+  unsigned char* prow = sP + tid * 128;
+#pragma unroll
+  for (int c = 0; c < kBlkMaxKeys / 8; ++c) {
+    if (c * 8 < NK) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = exp2f(sc[c * 8 + 2 * e] - mb), p1 = exp2f(sc[c * 8 + 2 * e + 1] - mb);
+        lb += p0 + p1;
+        pk[e] = pack_bf16(p0, p1);
+      }
+      *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();  // every row's P is written and every S read
+  tc::fence_after_sync();
+  if (tid == 0) {
+    const uint32_t idesc = tc::idesc_bf16_f32(kBlkQ, HD) | (1u << 16);  // V is MN-major
+    for (int kk = 0; kk < NK / 16; ++kk) {
+      const uint64_t dp = tc::sw128_kmajor_desc(smem_addr(sP + kk * 32));
+      const uint64_t dv = tc::sw128_mnmajor_desc(smem_addr(sV + kk * 2048), KVH);
+      tc::mma_bf16(tmem, dp, dv, idesc, kk > 0 ? 1u : 0u);
+    }
+    tc::mma_commit(&bar[1]);
+  }
+  // merge weights of the block part and the prefix partial
+  float wb = 1.f, wp = 0.f, l = lb;
+  if (a.P > 0) {
+    const float M = fmaxf(mb, mp);
+    wb = exp2f(mb - M);
+    wp = exp2f(mp - M);
+    l = lb * wb + lp * wp;
+  }
+  const float inv = 1.f / l;
+  tc::mbar_wait(&bar[1], 0, a.err);
+  tc::fence_after_sync();
+  bf16* dst = reinterpret_cast<bf16*>(a.attn) + (size_t)(rb * L + vn) * a.ld_attn + (kvh * G + (live ? v % G : 0)) * HD;
+  float* po = a.part_o + qi * HD;
+  // correction mode: the row's merged state (max in log2 units, denominator,
+  // unnormalised output) replaces its prefix partial for the correction kernel
+  if (correct && live) {
+    a.part_ml[qi * 2] = a.P > 0 ? fmaxf(mb, mp) : mb;
+    a.part_ml[qi * 2 + 1] = l;
+  }
+#pragma unroll
+  for (int c0 = 0; c0 < HD; c0 += 32) {
+    float o[32];
+    tc::tmem_ld32(tl + c0, o);
+    if (live) {
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = o[c + e] * wb;
+        if (a.P > 0) {
+          const float4 p0 = *reinterpret_cast<const float4*>(po + c0 + c);
+          const float4 p1 = *reinterpret_cast<const float4*>(po + c0 + c + 4);
+          x[0] += wp * p0.x; x[1] += wp * p0.y; x[2] += wp * p0.z; x[3] += wp * p0.w;
+          x[4] += wp * p1.x; x[5] += wp * p1.y; x[6] += wp * p1.z; x[7] += wp * p1.w;
+        }
+        *reinterpret_cast<uint4*>(dst + c0 + c) =
+            make_uint4(pack_bf16(x[0] * inv, x[1] * inv), pack_bf16(x[2] * inv, x[3] * inv),
+                       pack_bf16(x[4] * inv, x[5] * inv), pack_bf16(x[6] * inv, x[7] * inv));
+        if (correct) {
+          *reinterpret_cast<float4*>(po + c0 + c) = make_float4(x[0], x[1], x[2], x[3]);
+          *reinterpret_cast<float4*>(po + c0 + c + 4) = make_float4(x[4], x[5], x[6], x[7]);
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, Lay::TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------ CUDA-core path (fp32 contexts)
 
 template <typename TAct>
@@ -1061,6 +1303,8 @@ __global__ void __launch_bounds__(128) attn_block_simt(const AttnArgs a) {
     raise_error(a.err, kErrAttn);
     return;
   }
+  // correction mode: only the rows that recompute (their own source)
+  if (a.mode == SF_ATTN_CORRECT && a.rc[g] != row) return;
   const TAct* qkv = reinterpret_cast<const TAct*>(a.qkv);
   for (int j = lane; j < hd; j += 32) qs[warp][j] = to_f32<TAct>(qkv[(size_t)g * a.ld_qkv + h * hd + j]);
   __syncwarp();
@@ -1107,6 +1351,113 @@ __global__ void __launch_bounds__(128) attn_block_simt(const AttnArgs a) {
   const float inv = 1.f / l;
   TAct* out = reinterpret_cast<TAct*>(a.attn) + (size_t)row * a.ld_attn + h * hd;
   for (int c = 0; c < per; ++c) out[lane + 32 * c] = from_f32<TAct>(acc[c] * inv);
+  if (a.mode == SF_ATTN_CORRECT) {
+    // the merged state replaces the first split's prefix partial (index
+    // slot * nq + head), which only this row read
+    __syncwarp();
+    const size_t qi = (size_t)g * a.nq + h;
+    for (int c = 0; c < per; ++c) a.part_o[qi * hd + lane + 32 * c] = acc[c];
+    if (lane == 0) {
+      a.part_ml[qi * 2] = M;
+      a.part_ml[qi * 2 + 1] = l;
+    }
+  }
+}
+
+// The subtract/add correction of a folded row ("SpecFold" §A.1, applied
+// against the nearest recomputed ancestor as in §A.3): one warp per (row,
+// query head).  The row's source row recomputed its query and left its merged
+// softmax state (max M in log2 units, denominator l, unnormalised output acc)
+// over the shared prefix and the source branch's block keys.  At the block
+// positions where the row's own branch reads a different key/value slot than
+// the source branch, the source's contribution is removed and the branch's
+// own added:
+//   M' = max(M, new scores);  l' = l 2^(M-M') - sum 2^(s_old-M') + sum 2^(s_new-M')
+//   acc' = acc 2^(M-M') - sum 2^(s_old-M') v_old + sum 2^(s_new-M') v_new
+// and the output is acc' / l'.  Recompute rows were written by the block
+// kernel and are skipped.
+template <typename TAct>
+__global__ void __launch_bounds__(128) attn_correct_kernel(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * 4 + warp;
+  const int row = w / a.nq, h = w % a.nq;
+  if (row >= a.T) return;
+  const int count = a.meta[0];
+  const int g = a.rcslot[row];
+  if (g < 0 || g >= count) {
+    raise_error(a.err, kErrAttn);
+    return;
+  }
+  const int srow = a.rc[g];
+  if (srow == row) return;  // a recompute row
+  if (srow < 0 || srow >= a.T) {
+    raise_error(a.err, kErrAttn);
+    return;
+  }
+  const int G = a.nq / a.nkv, kvh = h / G, hd = a.hd, per = hd / 32, L = a.L;
+  const int base_i = (row / L) * L, base_s = (srow / L) * L;
+  const TAct* qkv = reinterpret_cast<const TAct*>(a.qkv);
+  float q[kMaxHd / 32];
+  for (int c = 0; c < per; ++c) q[c] = to_f32<TAct>(qkv[(size_t)g * a.ld_qkv + h * hd + lane + 32 * c]);
+  const size_t qi = (size_t)g * a.nq + h;
+  const float M = a.part_ml[qi * 2], l0 = a.part_ml[qi * 2 + 1];
+  // block positions whose key/value slot differs between the branch and the source branch
+  int ki[2] = {0, 0}, ks[2] = {0, 0};
+  unsigned dmask[2] = {0u, 0u};
+  for (int rr = 0; rr < 2; ++rr) {
+    const int m = lane + 32 * rr;
+    bool diff = false;
+    if (m < L) {
+      ki[rr] = a.rcslot[base_i + m];
+      ks[rr] = a.rcslot[base_s + m];
+      diff = ki[rr] != ks[rr];
+    }
+    dmask[rr] = __ballot_sync(0xffffffffu, diff);
+  }
+  const int koff = (a.nq + kvh) * hd, voff = (a.nq + a.nkv + kvh) * hd;
+  auto score = [&](int slot) {
+    const TAct* kr = qkv + (size_t)slot * a.ld_qkv + koff;
+    float dot = 0.f;
+    for (int c = 0; c < per; ++c) dot += q[c] * to_f32<TAct>(kr[lane + 32 * c]);
+    return warp_sum(dot) * a.scale_log2;
+  };
+  // pass 1: the scores at the changed positions (lane m % 32 keeps those of position m)
+  float s_old[2] = {0.f, 0.f}, s_new[2] = {0.f, 0.f};
+  float Mn = M;
+  for (int rr = 0; rr < 2; ++rr) {
+    for (unsigned mk = dmask[rr]; mk; mk &= mk - 1) {
+      const int t = __ffs(mk) - 1;
+      const float so = score(__shfl_sync(0xffffffffu, ks[rr], t));
+      const float sn = score(__shfl_sync(0xffffffffu, ki[rr], t));
+      if (lane == t) {
+        s_old[rr] = so;
+        s_new[rr] = sn;
+      }
+      Mn = fmaxf(Mn, sn);
+    }
+  }
+  // pass 2: rescale to the new max, remove the old contributions, add the new
+  const float f = exp2f(M - Mn);
+  float l = l0 * f;
+  float acc[kMaxHd / 32];
+  for (int c = 0; c < per; ++c) acc[c] = a.part_o[qi * hd + lane + 32 * c] * f;
+  for (int rr = 0; rr < 2; ++rr) {
+    for (unsigned mk = dmask[rr]; mk; mk &= mk - 1) {
+      const int t = __ffs(mk) - 1;
+      const float wo = exp2f(__shfl_sync(0xffffffffu, s_old[rr], t) - Mn);
+      const float wn = exp2f(__shfl_sync(0xffffffffu, s_new[rr], t) - Mn);
+      const TAct* vo = qkv + (size_t)__shfl_sync(0xffffffffu, ks[rr], t) * a.ld_qkv + voff;
+      const TAct* vn = qkv + (size_t)__shfl_sync(0xffffffffu, ki[rr], t) * a.ld_qkv + voff;
+      l += wn - wo;
+      for (int c = 0; c < per; ++c)
+        acc[c] += wn * to_f32<TAct>(vn[lane + 32 * c]) - wo * to_f32<TAct>(vo[lane + 32 * c]);
+    }
+  }
+  const float inv = 1.f / l;
+  TAct* out = reinterpret_cast<TAct*>(a.attn) + (size_t)row * a.ld_attn + h * hd;
+  for (int c = 0; c < per; ++c) out[lane + 32 * c] = from_f32<TAct>(acc[c] * inv);
 }
 
 template <int HD>
@@ -1125,6 +1476,8 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_prefix_mma<HD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                prefix_smem_bytes<HD, 4>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_block_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, BlkLayout<HD>::bytes(64));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_mma<HD, kKB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
@@ -1158,13 +1511,16 @@ cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
     }
     lc.after(SF_K_ATTN_PREFIX);
   }
-  dim3 grid((a.L * G + kBQT - 1) / kBQT, a.R * a.Bp * a.nkv);
+  dim3 grid((a.L * G + kBlkQ - 1) / kBlkQ, a.R * a.Bp * a.nkv);
   lc.before(SF_K_ATTN_BLOCK);
-  if (kb == 32)
-    lc.check(launch_pdl(lc.st, grid, dim3(64), smem_b, 1, attn_block_mma<HD, 32>, a));
-  else
-    lc.check(launch_pdl(lc.st, grid, dim3(64), smem_b, 1, attn_block_mma<HD, kKB>, a));
+  lc.check(launch_pdl(lc.st, grid, dim3(kBlkQ), (size_t)BlkLayout<HD>::bytes(a.L <= 32 ? 32 : 64), 1,
+                      attn_block_tc<HD>, a));
   lc.after(SF_K_ATTN_BLOCK);
+  if (a.mode == SF_ATTN_CORRECT) {
+    lc.before(SF_K_ATTN_CORRECT);
+    lc.check(launch_pdl(lc.st, dim3((a.T * a.nq + 3) / 4), dim3(128), 0, 1, attn_correct_kernel<bf16>, a));
+    lc.after(SF_K_ATTN_CORRECT);
+  }
   return lc.err;
 }
 
@@ -1179,6 +1535,11 @@ cudaError_t attention_simt(Launch& lc, const AttnArgs& a) {
   lc.before(SF_K_ATTN_BLOCK);
   lc.check(launch_pdl(lc.st, dim3((a.T * a.nq + 3) / 4), dim3(128), 0, 1, attn_block_simt<TAct>, a));
   lc.after(SF_K_ATTN_BLOCK);
+  if (a.mode == SF_ATTN_CORRECT) {
+    lc.before(SF_K_ATTN_CORRECT);
+    lc.check(launch_pdl(lc.st, dim3((a.T * a.nq + 3) / 4), dim3(128), 0, 1, attn_correct_kernel<TAct>, a));
+    lc.after(SF_K_ATTN_CORRECT);
+  }
   return lc.err;
 }
 

@@ -153,6 +153,45 @@ struct EpiStore {
   }
 };
 
+// Greedy-token partial of the LM head: for output row g and the 128 vocabulary
+// entries [m0, m0 + 128) of this tile, the largest logit and its index (the
+// lowest index on a tie; entries at or past `vocab` are zero padding of the
+// packed weight and are skipped), stored at part[g * ld + m0 / 128] as
+// (value, index bits).  All 32 lanes of the warp take part.
+struct EpiArgmax {
+  struct Params {
+    float2* part;
+    int ld;     // vocabulary tiles per row
+    int vocab;
+  };
+  struct Pre {};
+  static constexpr bool kStaged = false;
+  static __device__ __forceinline__ void prefetch(const Params&, int, int, int, Pre&) {}
+  static __device__ __forceinline__ void apply(const Params& p, int g, int m0, int lane, const float v[4],
+                                               const Pre&) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {  // features rise with c, so the first maximum wins
+      const int f = m0 + lane + 32 * c;
+      if (f < p.vocab && (v[c] > best || bi == 0x7fffffff)) {
+        best = v[c];
+        bi = f;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ob > best || (ob == best && oi < bi))) {
+        best = ob;
+        bi = oi;
+      }
+    }
+    if (lane == 0) p.part[(size_t)g * p.ld + (m0 >> 7)] = make_float2(best, __int_as_float(bi));
+  }
+};
+
 // Epilogue of up to 32 rows row0 + stride * jj, jj < nvalid; epilogue warp ew
 // handles jj = ew + 4b (b = 0..7).  epilogue_prefetch() issues the global reads
 // of all of them (it can run before the accumulators are ready, e.g. while the

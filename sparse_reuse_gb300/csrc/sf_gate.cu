@@ -206,32 +206,33 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
   uint8_t* flags = dyn;
   int* slot = reinterpret_cast<int*>(dyn + ((a.T + 15) & ~15));
   compact_and_resolve(a, flags, slot, tmp);
-  if (threadIdx.x == 0) *a.ticket = 0u;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *a.ticket = 0u;
+    // a resolution check that fired is reported through the count as well
+    if (a.rc_count_user && a.err && (atomicOr(a.err, 0u) & kErrGate)) *a.rc_count_user = -1;
+  }
 }
 
 // ---------------------------------------------------------------- fused gate
 
-// Completion tag of this layer's compaction: (pass epoch * 1024 + layer) * 2 + 1
-// is unique to this layer of this pass (at most 1024 layers) and never zero,
-// so the word needs no clearing between layers or passes.
-__device__ __forceinline__ unsigned done_tag(const GateArgs& a) {
+// Tag of this layer of this pass: (pass epoch * 1024 + layer) * 2 + 1 is
+// unique to it (at most 1024 layers) and never zero, so the rows' scan words
+// need no clearing between layers or passes.
+__device__ __forceinline__ unsigned scan_tag(const GateArgs& a) {
   return ((*a.epoch) * 1024u + (unsigned)a.layer) * 2u + 1u;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// A row's gate word: the layer's tag in the high half, and in bit 0 whether
+// the row recomputes.
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long gate_timer_ns() {
@@ -240,151 +241,290 @@ __device__ __forceinline__ unsigned long long gate_timer_ns() {
   return t;
 }
 
-constexpr unsigned long long kDoneWaitNs = 2000000000ull;  // a wait that gives up raises kErrTimeout
+constexpr unsigned long long kScanWaitNs = 2000000000ull;  // a wait that gives up raises kErrTimeout
 
-// Gate, attention RMSNorm, compaction and source resolution of one layer in
-// one launch, one CTA per row (r, i, n):
-//   1. the row's layer input H (previous layer's residual applied) and its
-//      gate decision against the parent row;
-//   2. the CTA that takes the last ticket compacts and resolves every row
-//      (compact_and_resolve) and then sets the layer's completion tag;
-//   3. a recompute row's CTA waits for that tag, reads its slot and writes its
-//      normalised row there (folded rows' CTAs leave after step 1).
-// Only CTAs that already took a ticket wait, and they wait for the CTA that
-// took the last one, so the wait always ends; it is bounded all the same.
-// Short rows (VEC > 0) stay in registers; long rows (VEC == 0) are kept in
-// dynamic shared memory until their slot is known.
-template <bool kLayer0, typename TIn, int VEC, typename TAct>
-__global__ void __launch_bounds__(kGateThreads) gate_norm_kernel(const __grid_constant__ GateArgs a) {
-  __shared__ float red[32];
-  __shared__ int tmp[32];
-  __shared__ int s_fold, s_last, s_slot;
-  extern __shared__ __align__(16) unsigned char dyn[];
+// Whether row j recomputes (bit 0 of its word, once the word carries this
+// layer's tag; spinning, bounded).  `v` is a first read of the word.  A wait
+// that gives up raises kErrTimeout and answers "recomputes", so the caller
+// still finishes with in-range values.
+__device__ __noinline__ unsigned gate_word_wait(const GateArgs& a, int j, unsigned tag, unsigned long long v) {
+  const unsigned long long t0 = gate_timer_ns();
+  while ((unsigned)(v >> 32) != tag) {
+    __nanosleep(64);
+    v = ld_acquire_u64(a.scan + j);
+    if ((unsigned)(v >> 32) != tag && gate_timer_ns() - t0 > kScanWaitNs) {
+      raise_error(a.err, kErrTimeout);
+      return 1u;
+    }
+  }
+  return (unsigned)v & 1u;
+}
+
+__device__ __forceinline__ unsigned gate_word(const GateArgs& a, int j, unsigned tag) {
+  const unsigned long long v = ld_acquire_u64(a.scan + j);
+  return (unsigned)(v >> 32) == tag ? ((unsigned)v & 1u) : gate_word_wait(a, j, tag, v);
+}
+
+// Gate, part 1: the layer input and the gate decision of every row.  CTA =
+// one row, VEC float4 columns per thread (256 threads cover rows of up to
+// VEC * 1024 features), every load of the row and of its parent row issued
+// before the first is used: the row's layer input H (previous layer's
+// residual applied, written out), ||H - H_parent||^2, ||H_parent||^2 and
+// ||H||^2, the fold decision, and the row's gate word (release).  Nothing
+// here waits, so every CTA finishes whatever else is resident.
+template <bool kLayer0, typename TIn, int VEC>
+__global__ void __launch_bounds__(kGateThreads) gate_rows_kernel(const __grid_constant__ GateArgs a) {
+  __shared__ float red[3][32];
   pdl_wait();
   pdl_trigger();
-
   const int row = blockIdx.x;
   const int L = a.L, Bp = a.tree.Bp;
   const int n = row % L, rb = row / L, i = rb % Bp, r = rb / Bp;
   const int prow = i > 0 ? (r * Bp + a.tree.parent[r * Bp + i]) * L + n : -1;
   const int d4 = a.d >> 2;
-  float4* xrow = reinterpret_cast<float4*>(dyn);
-  unsigned char* cscratch = dyn + (VEC > 0 ? 0 : (size_t)a.d * sizeof(float));  // compaction's shared memory
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  float diff2 = 0.f, par2 = 0.f, ss = 0.f;
-  float4 xs[VEC > 0 ? VEC : 1];
-  if constexpr (VEC > 0) {
-    float4 ys[VEC];
+  float4 xs[VEC], ys[VEC];
+  if constexpr (kLayer0) {
+    const TIn* xr = reinterpret_cast<const TIn*>(a.x_in) + (size_t)row * a.d;
+    const TIn* yr = reinterpret_cast<const TIn*>(a.x_in) + (size_t)(prow >= 0 ? prow : row) * a.d;
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
-      const int c = threadIdx.x + k * blockDim.x;
+      const int c = threadIdx.x + k * kGateThreads;
       if (c < d4) {
-        xs[k] = layer_input4<kLayer0, TIn>(a, row, c);
-        if (prow >= 0) ys[k] = layer_input4<kLayer0, TIn>(a, prow, c);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < VEC; ++k) {
-      const int c = threadIdx.x + k * blockDim.x;
-      if (c < d4) {
-        const float4 x = xs[k];
-        *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
-        if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
-        ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-        if (prow >= 0) {
-          const float4 y = ys[k];
-          const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
-          diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
-          par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
-        }
+        xs[k] = load4<TIn>(xr + c * 4);
+        if (prow >= 0) ys[k] = load4<TIn>(yr + c * 4);
       }
     }
   } else {
-    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
-      const float4 x = layer_input4<kLayer0, TIn>(a, row, c);
+    // the previous layer's last residual add: H = h + f[source slot]; the
+    // parent's input is recomputed from the same operands, so it is
+    // bit-identical to what the parent's CTA writes
+    const float4* hx = reinterpret_cast<const float4*>(a.h_prev + (size_t)row * a.d);
+    const float4* fx = reinterpret_cast<const float4*>(a.f_prev + (size_t)a.rcslot_prev[row] * a.d);
+    const float4* hy = reinterpret_cast<const float4*>(a.h_prev + (size_t)(prow >= 0 ? prow : row) * a.d);
+    const float4* fy =
+        reinterpret_cast<const float4*>(a.f_prev + (size_t)a.rcslot_prev[prow >= 0 ? prow : row] * a.d);
+    float4 fxs[VEC], fys[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * kGateThreads;
+      if (c < d4) {
+        xs[k] = hx[c];
+        fxs[k] = fx[c];
+        if (prow >= 0) {
+          ys[k] = hy[c];
+          fys[k] = fy[c];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      xs[k] = make_float4(xs[k].x + fxs[k].x, xs[k].y + fxs[k].y, xs[k].z + fxs[k].z, xs[k].w + fxs[k].w);
+      if (prow >= 0)
+        ys[k] = make_float4(ys[k].x + fys[k].x, ys[k].y + fys[k].y, ys[k].z + fys[k].z, ys[k].w + fys[k].w);
+    }
+  }
+  float diff2 = 0.f, par2 = 0.f, ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    const int c = threadIdx.x + k * kGateThreads;
+    if (c < d4) {
+      const float4 x = xs[k];
       *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
       if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
-      xrow[c] = x;
       ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
       if (prow >= 0) {
-        const float4 y = layer_input4<kLayer0, TIn>(a, prow, c);
+        const float4 y = ys[k];
         const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
         diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
         par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
       }
     }
   }
-  if (prow >= 0) {
-    diff2 = block_sum(diff2, red);
-    par2 = block_sum(par2, red);
-  }
-  ss = block_sum(ss, red);
-  if (threadIdx.x == 0) {
-    // rho <= delta  <=>  ||diff||^2 <= delta^2 ||parent||^2 (covers a zero parent)
-    const int f = (prow >= 0 && a.delta > 0.f && diff2 <= a.delta * a.delta * par2) ? 1 : 0;
-    a.fold[row] = (uint8_t)f;
-    if (a.fold_user) a.fold_user[row] = (uint8_t)f;
-    s_fold = f;
-    // the ticket releases the flag to the CTA that takes the last one, which
-    // acquires every earlier ticket's flag
-    s_last = atom_add_acq_rel_gpu(a.ticket, 1u) == gridDim.x - 1;
+  // the three sums in one exchange, added in the same order as block_sum
+  diff2 = warp_sum(diff2);
+  par2 = warp_sum(par2);
+  ss = warp_sum(ss);
+  if (lane == 0) {
+    red[0][warp] = diff2;
+    red[1][warp] = par2;
+    red[2][warp] = ss;
   }
   __syncthreads();
-  const int f = s_fold;
-  const unsigned tag = done_tag(a);
-  if (s_last) {
-    uint8_t* flags = cscratch;
-    int* slot = reinterpret_cast<int*>(cscratch + ((a.T + 15) & ~15));
-    compact(a, flags, slot, tmp);
-    if (threadIdx.x == 0) {
-      *a.ticket = 0u;
-      s_slot = slot[row];
-      // after compact's closing block barrier this release covers every
-      // thread's writes of the list, the recompute rows' slots and the offsets
-      // (a failure-injection pass leaves the tag unset: the waits run out)
-      if (!a.stall) st_release_gpu(a.done, tag);
-    }
-    // the folded rows' sources are resolved while the recompute rows write
-    resolve(a, flags, slot);
-    __syncthreads();
-  } else {
-    if (f) return;
-    if (threadIdx.x == 0) {
-      unsigned long long t0 = 0;
-      while (ld_acquire_gpu(a.done) != tag) {
-        const unsigned long long t = gate_timer_ns();
-        if (t0 == 0) t0 = t;
-        if (t - t0 > kDoneWaitNs) {
-          raise_error(a.err, kErrTimeout);
-          break;
-        }
-        __nanosleep(32);
-      }
-      s_slot = __ldcg(a.rcslot + row);  // a recompute row is its own source
-    }
-    __syncthreads();
-  }
-  if (f) return;
-  const int sl = s_slot;
-  const float rstd = rsqrtf(ss / (float)a.d + a.eps);
-  TAct* out = reinterpret_cast<TAct*>(a.xn) + (size_t)sl * a.d;
-  if constexpr (VEC > 0) {
+  if (threadIdx.x != 0) return;
+  constexpr int kWarps = kGateThreads / 32;
+  diff2 = par2 = ss = 0.f;
+  // thread 0 adds the warps' sums as a warp_sum over lanes 0..7 would:
+  // pairwise at distance 16, 8, 4, 2, 1 (zeros above lane 7)
+  float d8[kWarps], p8[kWarps], s8[kWarps];
 #pragma unroll
-    for (int k = 0; k < VEC; ++k) {
-      const int c = threadIdx.x + k * blockDim.x;
-      if (c < d4) {
-        const float4 v = xs[k];
-        const float4 w = *reinterpret_cast<const float4*>(a.gain + c * 4);
-        store4<TAct>(out + c * 4, make_float4(v.x * rstd * w.x, v.y * rstd * w.y, v.z * rstd * w.z, v.w * rstd * w.w));
+  for (int w = 0; w < kWarps; ++w) {
+    d8[w] = red[0][w];
+    p8[w] = red[1][w];
+    s8[w] = red[2][w];
+  }
+#pragma unroll
+  for (int o = kWarps / 2; o > 0; o >>= 1)
+#pragma unroll
+    for (int w = 0; w < o; ++w) {
+      d8[w] += d8[w + o];
+      p8[w] += p8[w + o];
+      s8[w] += s8[w + o];
+    }
+  diff2 = d8[0];
+  par2 = p8[0];
+  ss = s8[0];
+  // rho <= delta  <=>  ||diff||^2 <= delta^2 ||parent||^2 (covers a zero parent)
+  const int f = (prow >= 0 && a.delta > 0.f && diff2 <= a.delta * a.delta * par2) ? 1 : 0;
+  a.fold[row] = (uint8_t)f;
+  if (a.fold_user) a.fold_user[row] = (uint8_t)f;
+  if (a.rho_user)
+    a.rho_user[row] = prow < 0 ? __int_as_float(0x7fc00000)
+                               : (par2 > 0.f ? sqrtf(diff2 / par2) : (diff2 > 0.f ? __int_as_float(0x7f800000) : 0.f));
+  a.row_ss[row] = ss;
+  // the release covers this row's H, which the CTA's barrier ordered before
+  // it, and its sums
+  __threadfence();
+  if (!(a.stall && row == 0))  // failure injection: row 0 never reports
+    st_release_u64(a.scan + row, ((unsigned long long)scan_tag(a) << 32) | (f ? 0u : 1u));
+}
+
+// Gate, part 2: compaction, source resolution and attention RMSNorm.  CTA =
+// one row.  It starts while part 1 still runs (it lets its own dependants go
+// at once and waits for part 1's completion only before it exits), and
+// reads part 1's results through the rows' gate words (acquire, bounded
+// spin): part 1 has all its CTAs running before this grid can start, and
+// they never wait, so every word arrives.
+//   - a folded row follows its chain up the tree (the ancestors are lower
+//     rows at the same position) to the nearest ancestor that recomputes;
+//   - the CTA counts the recompute rows below the row, and below its source,
+//     from the words of all lower rows (256 threads read them at once): the
+//     counts are the slots of the row and of its source in the stable
+//     ascending recompute list;
+//   - a recompute row writes its list entry and its normalised row at its
+//     slot (H from part 1, through L2).
+template <typename TAct>
+__global__ void __launch_bounds__(kGateThreads) gate_compact_kernel(const __grid_constant__ GateArgs a) {
+  __shared__ int cnt[2][32];
+  __shared__ int s_srow, s_src, s_slot;
+  pdl_trigger();
+  const int row = blockIdx.x;
+  const int L = a.L, Bp = a.tree.Bp;
+  const int n = row % L, rb = row / L, i = rb % Bp, r = rb / Bp;
+  const unsigned tag = scan_tag(a);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = kGateThreads / 32;
+
+  if (warp == 0) {
+    // lane k reads the word of the k-th row up the chain (the row itself,
+    // its parent's row, ...; 32 at a time); the source is the nearest one
+    // that recomputes, and the main branch always does
+    int start = i;
+    for (;;) {
+      int b = start;
+      for (int k = 0; k < lane && b >= 0; ++k) b = a.tree.parent[r * Bp + b];
+      const bool on = b >= 0;
+      const unsigned rc = on ? gate_word(a, (r * Bp + b) * L + n, tag) : 0u;
+      const unsigned hits = __ballot_sync(0xffffffffu, on && rc);
+      if (hits) {
+        const int src = __shfl_sync(0xffffffffu, b, __ffs(hits) - 1);
+        if (lane == 0) {
+          s_srow = (r * Bp + src) * L + n;
+          s_src = src;
+        }
+        break;
+      }
+      const int next = __shfl_sync(0xffffffffu, b, 31);
+      if (next < 0 || __shfl_sync(0xffffffffu, on, 31) == 0) {  // cannot happen for a validated tree
+        if (lane == 0) {
+          raise_error(a.err, kErrGate);
+          s_srow = r * Bp * L + n;
+          s_src = 0;
+        }
+        break;
+      }
+      start = a.tree.parent[r * Bp + next];
+      if (start < 0) {
+        if (lane == 0) {
+          raise_error(a.err, kErrGate);
+          s_srow = r * Bp * L + n;
+          s_src = 0;
+        }
+        break;
       }
     }
-  } else {
-    for (int c = threadIdx.x; c < d4; c += blockDim.x) {
-      const float4 v = xrow[c];
+  }
+  __syncthreads();
+  const int srow = s_srow;
+  const bool own = srow == row;
+  // recompute rows below this row and below the source row, 4 words a thread at a time
+  int below = 0, below_src = 0;
+  for (int j0 = 0; j0 < row; j0 += 4 * kGateThreads) {
+    unsigned long long w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = j0 + threadIdx.x + k * kGateThreads;
+      w[k] = j < row ? ld_acquire_u64(a.scan + j) : 0ull;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = j0 + threadIdx.x + k * kGateThreads;
+      if (j < row) {
+        const unsigned rc = (unsigned)(w[k] >> 32) == tag ? ((unsigned)w[k] & 1u) : gate_word_wait(a, j, tag, w[k]);
+        below += rc;
+        below_src += j < srow ? rc : 0;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    below += __shfl_xor_sync(0xffffffffu, below, o);
+    below_src += __shfl_xor_sync(0xffffffffu, below_src, o);
+  }
+  if (lane == 0) {
+    cnt[0][warp] = below;
+    cnt[1][warp] = below_src;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tot = 0, tot_src = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      tot += cnt[0][w];
+      tot_src += cnt[1][w];
+    }
+    const int slot = own ? tot : tot_src;
+    if (own) {
+      a.rc[slot] = row;
+      if (a.rc_user) a.rc_user[slot] = row;
+      if (i == 0 && n == 0) a.meta[1 + r] = slot;  // first recompute row of request r
+    }
+    a.rcslot[row] = slot;
+    if (a.src_user) a.src_user[row] = s_src;
+    if (row == a.T - 1) {
+      const int total = tot + (own ? 1 : 0);
+      a.meta[0] = total;
+      a.meta[1 + a.tree.R] = total;
+      if (a.rc_count_user) *a.rc_count_user = total;
+    }
+    s_slot = slot;
+  }
+  __syncthreads();
+  if (own) {
+    const int sl = s_slot;
+    const float rstd = rsqrtf(__ldcg(a.row_ss + row) / (float)a.d + a.eps);
+    const float4* Hrow = reinterpret_cast<const float4*>(a.H_out + (size_t)row * a.d);
+    TAct* out = reinterpret_cast<TAct*>(a.xn) + (size_t)sl * a.d;
+    for (int c = threadIdx.x; c < (a.d >> 2); c += kGateThreads) {
+      const float4 v = __ldcg(Hrow + c);
       const float4 w = *reinterpret_cast<const float4*>(a.gain + c * 4);
       store4<TAct>(out + c * 4, make_float4(v.x * rstd * w.x, v.y * rstd * w.y, v.z * rstd * w.z, v.w * rstd * w.w));
     }
   }
+  // part 1 has completed before this grid does, so every kernel after this
+  // one sees both grids finished when its own dependency wait returns
+  pdl_wait();
 }
 
 // RMSNorm of rows rc[g] (or g when rc is null), g < count, gathered into a
@@ -505,32 +645,36 @@ cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16) {
 
 namespace {
 
-template <int VEC, typename TAct>
-cudaError_t launch_gate_norm_vec(Launch& lc, const GateArgs& a, int bf16) {
-  // the long row (VEC == 0), then the compaction's flags and slots
-  const size_t dyn =
-      (VEC > 0 ? 0 : (size_t)a.d * sizeof(float)) + (size_t)((a.T + 15) & ~15) + (size_t)a.T * sizeof(int);
-  auto k0 = a.x_in == nullptr ? gate_norm_kernel<false, float, VEC, TAct>
-                              : (bf16 ? gate_norm_kernel<true, __nv_bfloat16, VEC, TAct>
-                                      : gate_norm_kernel<true, float, VEC, TAct>);
-  if (dyn > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), dyn, 1, k0, a);
+template <int VEC>
+cudaError_t launch_gate_rows(Launch& lc, const GateArgs& a, int bf16) {
+  // layer 0 reads the block input, which has the context dtype
+  auto k = a.x_in == nullptr ? gate_rows_kernel<false, float, VEC>
+                             : (bf16 ? gate_rows_kernel<true, __nv_bfloat16, VEC> : gate_rows_kernel<true, float, VEC>);
+  return launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), 0, 1, k, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gate_norm(Launch& lc, const GateArgs& a, int bf16) {
-  if (a.d % 4 != 0 || !a.xn || !a.gain || !a.done || !a.epoch || !a.ticket) return lc.err = cudaErrorInvalidValue;
-  const int d4 = a.d / 4;
+  const int per = (a.d / 4 + kGateThreads - 1) / kGateThreads;  // float4 columns a thread
+  if (a.d % 4 != 0 || per > 16 || !a.xn || !a.gain || !a.scan || !a.epoch || !a.row_ss || a.T < 1)
+    return lc.err = cudaErrorInvalidValue;
+  // two launches, each bracketed (counted and, when selected, timed) on its own
   lc.before(SF_K_GATE);
-  if (bf16)
-    lc.check(d4 <= 512 ? launch_gate_norm_vec<2, __nv_bfloat16>(lc, a, bf16)
-                       : launch_gate_norm_vec<0, __nv_bfloat16>(lc, a, bf16));
+  if (per <= 2)
+    lc.check(launch_gate_rows<2>(lc, a, bf16));
+  else if (per <= 4)
+    lc.check(launch_gate_rows<4>(lc, a, bf16));
+  else if (per <= 6)
+    lc.check(launch_gate_rows<6>(lc, a, bf16));
+  else if (per <= 8)
+    lc.check(launch_gate_rows<8>(lc, a, bf16));
   else
-    lc.check(d4 <= 512 ? launch_gate_norm_vec<2, float>(lc, a, bf16) : launch_gate_norm_vec<0, float>(lc, a, bf16));
+    lc.check(launch_gate_rows<16>(lc, a, bf16));
+  lc.after(SF_K_GATE);
+  lc.before(SF_K_GATE);
+  lc.check(launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), 0, 1,
+                      bf16 ? gate_compact_kernel<__nv_bfloat16> : gate_compact_kernel<float>, a));
   lc.after(SF_K_GATE);
   return lc.err;
 }
@@ -600,7 +744,9 @@ std::mutex g_scratch_mu;
 unsigned char* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_gate_scratch on the current device (looked up once per
-// device; the host-side symbol itself is not a device address).
+// device; the host-side symbol itself is not a device address).  The cached
+// address belongs to the device's primary context: it does not survive a
+// device reset, after which the library must be reloaded.
 cudaError_t gate_scratch(unsigned char** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

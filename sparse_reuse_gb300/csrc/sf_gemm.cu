@@ -115,6 +115,11 @@ cudaError_t gemm_simt(Launch& lc, int fam, const GemmArgs& g, EpiKind kind, cons
       lc.check(launch_pdl(lc.st, dim3(blocks), dim3(128), 0, 1, epilogue_kernel<EpiStore>, (const float*)y32, ldy, n_tiles, g.count, g.dense_count, p));
       break;
     }
+    case kEpiArgmax: {
+      EpiArgmax::Params p{e.part, e.part_ld, e.vocab};
+      lc.check(launch_pdl(lc.st, dim3(blocks), dim3(128), 0, 1, epilogue_kernel<EpiArgmax>, (const float*)y32, ldy, n_tiles, g.count, g.dense_count, p));
+      break;
+    }
   }
   lc.after(SF_K_AUX);
   return lc.err;

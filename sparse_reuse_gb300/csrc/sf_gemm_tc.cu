@@ -488,6 +488,9 @@ cudaError_t launch_gemm_tc(Launch& lc, int fam, const TcGemm& g, EpiKind kind, c
     case kEpiStore:
       err = launch_tc<EpiStore>(g, EpiStore::Params{e.y, e.y_ld}, lc.st);
       break;
+    case kEpiArgmax:
+      err = launch_tc<EpiArgmax>(g, EpiArgmax::Params{e.part, e.part_ld, e.vocab}, lc.st);
+      break;
   }
   if (err != cudaSuccess && lc.err == cudaSuccess) lc.err = err;
   lc.after(fam);

@@ -32,16 +32,19 @@ struct sf_graph_key {
   void* rc_count = nullptr;
   void* dbg_hidden = nullptr;
   void* dbg_rc = nullptr;
+  void* dbg_rho = nullptr;
   void* stream = nullptr;
   int R = 0, B = 0, P = 0;
   float delta = 0.f;
   int stall = 0;
+  int attn_mode = 0;
   std::vector<int> parent;
   bool operator==(const sf_graph_key& o) const {
     return hidden_in == o.hidden_in && prefix_k == o.prefix_k && prefix_v == o.prefix_v &&
            hidden_out == o.hidden_out && fold == o.fold && src == o.src && rc_count == o.rc_count &&
-           dbg_hidden == o.dbg_hidden && dbg_rc == o.dbg_rc && stream == o.stream && R == o.R &&
-           B == o.B && P == o.P && delta == o.delta && stall == o.stall && parent == o.parent;
+           dbg_hidden == o.dbg_hidden && dbg_rc == o.dbg_rc && dbg_rho == o.dbg_rho && stream == o.stream && R == o.R &&
+           B == o.B && P == o.P && delta == o.delta && stall == o.stall && attn_mode == o.attn_mode &&
+           parent == o.parent;
   }
 };
 
@@ -73,14 +76,18 @@ struct sf_ctx {
   int32_t* rcslot[2] = {nullptr, nullptr};  // [T_max], ping-pong between layers
   int32_t* meta = nullptr;  // [0] = rc count, [1 + r] = first recompute slot of request r
   unsigned* ticket = nullptr;
-  unsigned* epoch = nullptr;  // [0] pass counter, [1] completion tag of the gate's compaction
+  unsigned* epoch = nullptr;  // [0] pass counter
+  unsigned long long* scan = nullptr;  // [T_max] the gate's per-row words
+  float* gate_ss = nullptr;            // [T_max] ||H||^2 per row
   unsigned* err_dev = nullptr;
   unsigned* err_host = nullptr;  // pinned mirror, refreshed at the end of every pass
   float2* rope = nullptr;   // [max_pos][hd/2] (cos, sin), computed in double on the host
 
   float* dbg_hidden = nullptr;
   int32_t* dbg_rc = nullptr;
-  int inject_stall = 0;  // failure injection: layer 0's compaction never signals completion
+  float* dbg_rho = nullptr;  // [n_layers][T] gate rho dump, or nullptr
+  int inject_stall = 0;  // failure injection: layer 0's first row never reports its gate decision
+  int attn_mode = SF_ATTN_DIRECT;
 
   sf_stats stats{};
   bool use_graphs = true;
@@ -129,7 +136,7 @@ struct GemmArgs {
   bool count_early;        // count written two or more launches back (final when the grid starts)
 };
 
-enum EpiKind { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2, kEpiStore = 3 };
+enum EpiKind { kEpiQKV = 0, kEpiResidual = 1, kEpiSwiGLU = 2, kEpiStore = 3, kEpiArgmax = 4 };
 
 struct EpiArgs {
   // kEpiQKV
@@ -141,6 +148,8 @@ struct EpiArgs {
   void* u = nullptr; int u_ld = 0;
   // kEpiStore
   float* y = nullptr; int y_ld = 0;
+  // kEpiArgmax
+  float2* part = nullptr; int part_ld = 0; int vocab = 0;
 };
 
 struct GateArgs {
@@ -167,9 +176,11 @@ struct GateArgs {
   void* xn;               // [T_rc][d] context dtype: normalised recompute rows
   const float* gain;      // [d] attention RMSNorm gain
   float eps;
-  unsigned* done;         // completion tag of the layer's compaction
-  int stall;              // failure injection: the tag is never set, so its waits run out
-  const unsigned* epoch;  // pass counter, advanced by the final residual kernel
+  unsigned long long* scan;  // [T] per-row gate words (tag | recompute bit)
+  float* row_ss;             // [T] ||H||^2 of the row, for the attention RMSNorm
+  float* rho_user;           // [T] or nullptr: rho of every row (NaN for the main branch)
+  int stall;                 // failure injection: row 0 never reports, so the waits on it run out
+  const unsigned* epoch;     // pass counter, advanced by the final residual kernel
   int layer;
 };
 
@@ -218,6 +229,11 @@ struct AttnArgs {
   int target_ctas;  // prefix splits are chosen on the device to reach about this many CTAs
   float scale_log2;
   unsigned* err;
+  // SF_ATTN_CORRECT: the block kernels run only the recompute rows and leave
+  // their merged softmax state in part_o / part_ml (index slot * nq + head);
+  // the correction kernel derives every folded row from its source's state
+  int mode;
+  const int32_t* rc;  // recompute list (row of every slot)
 };
 cudaError_t launch_attention(Launch& lc, int act_bf16, const AttnArgs& a);
 

@@ -45,8 +45,8 @@ class Config:
     prefix_len: int = 512      # P
     n_requests: int = 1        # R
     n_drafts: int = 8          # B
-    tree: str = "random"       # "random" (depth <= max_depth) or "chain"
-    max_depth: int = 3
+    tree: str = "random"       # "random" (depth <= max_depth), "chain", "siblings" or "chains"
+    max_depth: int = 3         # "random": depth bound; "chains": length of each chain off the main branch
     unmask_max: int = 4        # S_t upper bound (uniform 1..unmask_max)
     unmask_exact: Optional[int] = None  # if set, every child unmasks exactly this many
     mask_frac: float = 0.5     # fraction of the main block still masked
@@ -82,6 +82,23 @@ CONFIGS = {
 
 DELTA_SWEEP_8B = (0.0, 0.01, 0.1, 0.2, 0.3, 0.7)
 DRAFT_SWEEP_14B = (2, 4, 6, 8)
+DEPTH_SWEEP = (1, 2, 3, 4)
+HEAD_VOCAB = 131072        # synthetic LM-head vocabulary of the benchmark (not a checkpoint's)
+
+
+def depth_config(base: Config, depth: int) -> Config:
+    """Drafting-strategy workload: a budget of B = 7 one-token drafts arranged
+    as chains of `depth` off the main branch, from seven siblings (depth 1) to
+    parent-extending chains (depth 4), every draft unmasking exactly one more
+    position than its parent."""
+    return base.with_(name=f"{base.name}-D{depth}", n_drafts=7, tree="chains", max_depth=depth, unmask_exact=1)
+
+
+def ripple_config(base: Config) -> Config:
+    """Residual-ripple workload: a main block with 17 of its 32 positions
+    committed (15 still masked) and one child that unmasks one more position."""
+    return base.with_(name=f"{base.name}-ripple", n_drafts=1, tree="chain", mask_frac=15 / 32, unmask_exact=1,
+                      block_len=32)
 
 
 def weight_seed(seed: int, layer: int, tensor: str) -> int:
@@ -126,6 +143,15 @@ def make_tree(cfg: Config, seed: int = 0, request: int = 0) -> np.ndarray:
     if cfg.tree == "siblings":
         p = np.zeros(Bp, dtype=np.int32)
         p[0] = -1
+        return p
+    if cfg.tree == "chains":
+        # drafts 1..B in chains of max_depth off the main branch, each draft
+        # extending the previous one of its chain (the last chain may be
+        # shorter): max_depth = 1 gives B siblings, max_depth = B one chain
+        p = np.empty(Bp, dtype=np.int32)
+        p[0] = -1
+        for i in range(1, Bp):
+            p[i] = 0 if (i - 1) % cfg.max_depth == 0 else i - 1
         return p
     rng = np.random.default_rng([seed, 7919, request])
     parent = [-1]
@@ -196,6 +222,15 @@ def make_prefix_kv(cfg: Config, seed: int = 0, device="cpu", n_layers: Optional[
         out.append((torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std)
                    .to(_torch_dtype(cfg)).contiguous())
     return out[0], out[1]
+
+
+def make_head_weights(cfg: Config, vocab: int, seed: int = 0, device="cpu"):
+    """Final RMSNorm gain (fp32 ones) and LM head [d, vocab] N(0, 0.02) in cfg.dtype."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000003 + 999_979)
+    w = (torch.randn((cfg.d_model, vocab), generator=g, device=device, dtype=torch.float32) * W_STD)
+    return torch.ones(cfg.d_model, dtype=torch.float32, device=device), w.to(_torch_dtype(cfg)).contiguous()
 
 
 @dataclass

@@ -25,3 +25,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+# One-line measured figures that GPU tests report (e.g. the free-running
+# bf16 drift); printed in the terminal summary so they appear at the end of a
+# quiet run.
+_SUMMARY = []
+
+
+@pytest.fixture
+def summary_line():
+    return _SUMMARY.append
+
+
+def pytest_terminal_summary(terminalreporter):
+    for line in _SUMMARY:
+        terminalreporter.write_line(line)

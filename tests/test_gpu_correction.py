@@ -1,0 +1,86 @@
+"""The pages' own attention mechanism (SpecFold summary §A.1 with §A.3):
+in SF_ATTN_CORRECT mode only recompute rows run the block attention, and a
+folded row is its source row's softmax state corrected by subtracting the
+source branch's contributions at the block positions where its own branch's
+keys differ and adding its own.  The result is defined to be the branch's
+exact attention, so the same oracle checks it as the direct mode (needs a
+GB300)."""
+import numpy as np
+import pytest
+
+import synth
+from parity import check_free_running, check_teacher_forced, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from sparse_reuse_gb300 import build
+    build.build()
+
+
+def _run(cfg, wl, delta, mode, debug=True):
+    import sparse_reuse_gb300 as sf
+    ctx = sf.from_config(cfg, wl.weights)
+    ctx.set_attention_mode(mode)
+    gpu = run_gpu(cfg, wl, delta, debug=debug, ctx=ctx)
+    ctx.sync()
+    st = ctx.stats()
+    ctx.close()
+    return gpu, st
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(n_drafts=6, tree="random", n_requests=2),
+                                dict(block_len=64, n_drafts=3, tree="random"), dict(prefix_len=0, n_drafts=4)])
+def test_fp32_correction_free_running(kw):
+    import sparse_reuse_gb300 as sf
+    cfg = synth.CONFIGS["tiny"].with_(**dict(dict(n_layers=2, prefix_len=37), **kw))
+    wl = synth.make_workload(cfg, seed=31, device="cuda")
+    gpu, st = _run(cfg, wl, 0.1, sf.SF_ATTN_CORRECT)
+    assert gpu["fold"].any()
+    assert st["family_launches"]["attn_correct"] == cfg.n_layers
+    check_free_running(cfg, wl, gpu, 0.1)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(n_requests=3, n_q_heads=7, n_kv_heads=1, prefix_len=200, n_drafts=4),
+                                dict(prefix_len=2100, head_dim=64, n_q_heads=8, n_kv_heads=2, block_len=20,
+                                     n_drafts=5)])
+def test_bf16_correction_teacher_forced(kw):
+    import sparse_reuse_gb300 as sf
+    base = dict(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=128, d_ffn=320, dtype="bf16",
+                block_len=32, prefix_len=96, n_drafts=4)
+    base.update(kw)
+    cfg = synth.small_config(**base)
+    wl = synth.make_workload(cfg, seed=32, device="cuda")
+    for delta in (0.0, 0.1):
+        gpu, _ = _run(cfg, wl, delta, sf.SF_ATTN_CORRECT)
+        check_teacher_forced(cfg, wl, gpu, delta, range(cfg.n_layers))
+
+
+def test_1p5b_correction_teacher_forced_all_layers():
+    import sparse_reuse_gb300 as sf
+    cfg = synth.CONFIGS["1.5b"]
+    wl = synth.make_workload(cfg, seed=0, device="cuda")
+    gpu, _ = _run(cfg, wl, cfg.delta, sf.SF_ATTN_CORRECT)
+    check_teacher_forced(cfg, wl, gpu, cfg.delta, range(cfg.n_layers))
+
+
+def test_14b_correction_sampled_layers():
+    import sparse_reuse_gb300 as sf
+    cfg = synth.CONFIGS["14b"]
+    wl = synth.make_workload(cfg, seed=0, device="cuda")
+    gpu, _ = _run(cfg, wl, cfg.delta, sf.SF_ATTN_CORRECT)
+    check_teacher_forced(cfg, wl, gpu, cfg.delta, [0, cfg.n_layers - 1])
+
+
+def test_modes_agree_on_the_first_layer():
+    """Same layer-0 input: the two mechanisms give the same attention up to
+    rounding, so the layer-1 inputs agree closely and the decisions match."""
+    import sparse_reuse_gb300 as sf
+    cfg = synth.CONFIGS["tiny"].with_(n_layers=1, n_drafts=5, tree="random")
+    wl = synth.make_workload(cfg, seed=33, device="cuda")
+    a, _ = _run(cfg, wl, 0.1, sf.SF_ATTN_DIRECT)
+    b, _ = _run(cfg, wl, 0.1, sf.SF_ATTN_CORRECT)
+    assert np.array_equal(a["fold"], b["fold"])
+    np.testing.assert_allclose(b["out"], a["out"], rtol=1e-5, atol=1e-6)

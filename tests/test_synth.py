@@ -48,3 +48,33 @@ def test_deterministic():
     assert np.array_equal(a.tokens, b.tokens)
     assert (a.hidden == b.hidden).all() and (a.prefix_k == b.prefix_k).all()
     assert all((a.weights[l][k] == b.weights[l][k]).all() for l in range(cfg.n_layers) for k in a.weights[l])
+
+
+def test_depth_sweep_trees():
+    """Drafting-strategy workload (SpecFold summary §D.2): B = 7 one-token
+    drafts, from seven siblings at depth 1 to parent-extending chains at 4."""
+    base = synth.CONFIGS["1.5b"]
+    for D in synth.DEPTH_SWEEP:
+        cfg = synth.depth_config(base, D)
+        p = synth.make_tree(cfg)
+        assert cfg.n_drafts == 7 and p[0] == -1
+        depth = [0]
+        for i in range(1, len(p)):
+            assert 0 <= p[i] < i
+            depth.append(depth[p[i]] + 1)
+        assert max(depth) == D
+        toks = synth.make_tokens(cfg, p)
+        for i in range(1, len(p)):
+            assert (toks[i] != toks[p[i]]).sum() == 1      # one more token than the parent
+    assert synth.make_tree(synth.depth_config(base, 1)).tolist() == [-1] + [0] * 7
+
+
+def test_ripple_workload():
+    """Residual-ripple workload (SpecFold summary §4.4): the parent has 17 of
+    32 positions committed and its only child unmasks one more."""
+    cfg = synth.ripple_config(synth.CONFIGS["1.5b"])
+    p = synth.make_tree(cfg)
+    toks = synth.make_tokens(cfg, p)
+    assert p.tolist() == [-1, 0]
+    assert (toks[0] != synth.MASK_ID).sum() == 17
+    assert (toks[1] != toks[0]).sum() == 1 and (toks[1] != synth.MASK_ID).sum() == 18
