@@ -146,11 +146,15 @@ sf_status sf_set_debug(sf_ctx* ctx, float* layer_hidden, int32_t* rc_rows);
  * does not go through this value. */
 sf_status sf_set_rho_dump(sf_ctx* ctx, float* rho);
 
-/* How a folded row's attention is computed (both give the branch's exact
+/* How a folded row's attention is computed (all give the branch's exact
  * attention; [SF] §A.1):
- *   SF_ATTN_DIRECT   every row attends to the shared prefix (through its
- *                    source query's prefix partial) and to its branch's own L
- *                    block keys (default);
+ *   SF_ATTN_DIRECT   every row attends to the shared prefix and to its
+ *                    branch's own L block keys (default).  Short prefixes run
+ *                    in one kernel that scores every row against both; longer
+ *                    ones keep one prefix partial per recomputed query and
+ *                    merge it with each row's block part;
+ *   SF_ATTN_DIRECT_SPLIT  the same with the prefix partial + block kernels
+ *                    whatever the prefix length (for comparison and tests);
  *   SF_ATTN_CORRECT  only recompute rows run the block attention, keeping
  *                    their merged softmax state (max, denominator, weighted
  *                    value sum); a folded row starts from its source row's
@@ -161,7 +165,7 @@ sf_status sf_set_rho_dump(sf_ctx* ctx, float* rho);
  *                    recomputed ancestor as in §A.3).
  * Applies to later sf_verify calls.  Errors: SF_ERR_INVALID_ARG (null ctx or
  * unknown mode). */
-typedef enum sf_attn_mode { SF_ATTN_DIRECT = 0, SF_ATTN_CORRECT = 1 } sf_attn_mode;
+typedef enum sf_attn_mode { SF_ATTN_DIRECT = 0, SF_ATTN_CORRECT = 1, SF_ATTN_DIRECT_SPLIT = 2 } sf_attn_mode;
 sf_status sf_set_attention_mode(sf_ctx* ctx, int mode);
 
 /* Wait for the context's work on `stream` to finish and report a device-side

@@ -23,7 +23,7 @@ SF_OK, SF_ERR_INVALID_ARG, SF_ERR_SHAPE, SF_ERR_TREE, SF_ERR_UNSUPPORTED, SF_ERR
 SF_F32, SF_BF16 = 0, 1
 FAMILIES = ["gate", "norm", "gemm_qkv", "attn_prefix", "attn_block", "gemm_o", "gemm_gateup", "gemm_down",
             "residual", "aux", "attn_correct"]
-SF_ATTN_DIRECT, SF_ATTN_CORRECT = 0, 1
+SF_ATTN_DIRECT, SF_ATTN_CORRECT, SF_ATTN_DIRECT_SPLIT = 0, 1, 2
 SF_K_COUNT = len(FAMILIES)
 
 # every symbol include/specfold.h declares

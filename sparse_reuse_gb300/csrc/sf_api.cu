@@ -61,8 +61,8 @@ void free_ctx(sf_ctx* c) {
     cudaFree(L.wqkv); cudaFree(L.wo); cudaFree(L.wgu); cudaFree(L.wd); cudaFree(L.g1); cudaFree(L.g2);
   }
   void* bufs[] = {c->H, c->h, c->fphys, c->xn, c->qkv, c->attn, c->u, c->y32, c->part_o, c->part_ml,
-                  c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->epoch, c->scan,
-                  c->gate_ss,
+                  c->fold, c->rc, c->rcslot[0], c->rcslot[1], c->meta, c->ticket, c->epoch, c->scan, c->gate_ss,
+
                   c->err_dev, c->rope};
   for (void* b : bufs) cudaFree(b);
   if (c->err_host) cudaFreeHost(c->err_host);
@@ -507,7 +507,8 @@ sf_status sf_set_debug(sf_ctx* c, float* layer_hidden, int32_t* rc_rows) {
 }
 
 sf_status sf_set_attention_mode(sf_ctx* c, int mode) {
-  if (!c || (mode != SF_ATTN_DIRECT && mode != SF_ATTN_CORRECT)) return SF_ERR_INVALID_ARG;
+  if (!c || (mode != SF_ATTN_DIRECT && mode != SF_ATTN_CORRECT && mode != SF_ATTN_DIRECT_SPLIT))
+    return SF_ERR_INVALID_ARG;
   c->attn_mode = mode;
   return SF_OK;
 }

@@ -6,22 +6,25 @@
 // onedev.kr review ("How to use it"): FlashAttention-style streaming, the
 // shared prefix KV seen by every branch through a zero-copy strided view, GQA.
 //
-// Decomposition used here (same result, different order of work):
-//   1. prefix partial per recomputed query: streaming softmax state
-//      (max, denominator, unnormalised output) of q against the request's
-//      prefix keys, the prefix split over S chunks;
-//   2. per (row, head): the query is the one of the row's resolved source;
-//      its block part runs over the branch's own L block keys/values, read
-//      through the source slots of the branch's positions, and is merged with
-//      the query's prefix partials by log-sum-exp.
-// The tensor-core path fixes the split count S from the prefix length (a
-// cluster of S CTAs per query tile); the CUDA-core path derives S on the
-// device from the live recompute count, identically in both of its kernels.
-//
-// BF16 contexts run both kernels on the tensor cores (mma.sync m16n8k16, bf16
-// in, fp32 accumulate); the GQA group's query heads are packed into the M
-// dimension so every key/value tile is read once per KV head.  FP32 contexts
-// use CUDA-core kernels that keep fp32 operands.
+// Kernels (BF16 contexts on the 5th-generation tensor cores, tcgen05 MMAs
+// into tensor memory; FP32 contexts on CUDA cores with fp32 operands):
+//   short prefixes, direct mode: one fused kernel per (branch, KV head, query
+//     tile): every row's query against the shared prefix (TMA-streamed) and
+//     against its branch's own block keys (gathered through the source slots),
+//     one streaming softmax, the normalised output written directly;
+//   otherwise:
+//     1. prefix partial per recomputed query: streaming softmax state
+//        (max, denominator, unnormalised output) of q against the request's
+//        prefix keys, the prefix split over S chunks (a cluster of S CTAs per
+//        query tile);
+//     2. per (row, head): the query is the one of the row's resolved source;
+//        its block part runs over the branch's own L block keys/values, read
+//        through the source slots of the branch's positions, and is merged
+//        with the query's prefix partial by log-sum-exp;
+//   SF_ATTN_CORRECT: step 2 for the recompute rows only, then the §A.1
+//     subtract/add correction for the folded rows.
+// The GQA group's query heads are packed into the M dimension so every
+// key/value tile is read once per KV head.
 #include "sf_internal.h"
 #include "sf_tc.cuh"
 
@@ -30,31 +33,13 @@ namespace {
 
 constexpr int kMaxHd = 128;
 constexpr int kMaxSplits = 8;
-constexpr int kQT = 64;  // query vectors per CTA (16 per warp)
+constexpr int kQT = 64;  // query tile of the CUDA-core path's split count
 constexpr int kKB = 64;  // keys per block
 
 // Number of prefix splits and keys per split for this pass.
 struct Splits {
   int S, len;
 };
-
-// Tensor-core path: the split count is fixed on the host from the prefix
-// length alone, so the split CTAs of a query tile form a cluster of exactly
-// that size.  Up to 512 keys a split is two 64-key blocks (more CTAs for a
-// short, latency-bound job); longer prefixes take four blocks per split,
-// which halves the partial states the cluster exchanges and merges.
-__host__ __device__ __forceinline__ int keys_per_split(int P) { return P <= 512 ? 128 : 256; }
-// K/V stages of the mma.sync prefix kernel: every block of a split is in
-// flight before the dependency wait.
-__host__ __device__ __forceinline__ int mma_prefix_stages(int P) { return keys_per_split(P) / 64; }
-__host__ __device__ __forceinline__ Splits fixed_splits(int P) {
-  if (P <= 0) return {0, 0};
-  const int kps = keys_per_split(P);
-  int S = (P + kps - 1) / kps;
-  S = S < 1 ? 1 : (S > kMaxSplits ? kMaxSplits : S);
-  const int len = (((P + S - 1) / S) + kKB - 1) / kKB * kKB;
-  return {(P + len - 1) / len, len};
-}
 
 __device__ __forceinline__ Splits prefix_splits(const AttnArgs& a) {
   if (a.P <= 0) return {0, 0};
@@ -86,364 +71,12 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float quad_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-}
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  return v + __shfl_xor_sync(0xffffffffu, v, 2);
-}
-
 using bf16 = __nv_bfloat16;
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float x, float y) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float x) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(x) : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Scores of this warp's 16 query rows against KB keys in smem (rows = keys).
-template <int HD, int KB>
-__device__ __forceinline__ void qk_scores(float (&sc)[KB / 8][4], const uint32_t (&qf)[HD / 16][4], const bf16* K,
-                                          int lane) {
-  constexpr int LD = HD + 8;
-#pragma unroll
-  for (int nt = 0; nt < KB / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-  const int j = lane >> 3;
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-#pragma unroll
-    for (int n2 = 0; n2 < KB / 16; ++n2) {
-      uint32_t kf[4];
-      ldsm_x4(kf, K + (n2 * 16 + (j >> 1) * 8 + (lane & 7)) * LD + kk * 16 + (j & 1) * 8);
-      mma16816(sc[2 * n2], qf[kk], kf[0], kf[1]);
-      mma16816(sc[2 * n2 + 1], qf[kk], kf[2], kf[3]);
-    }
-  }
-}
-
-// o += P V for this warp's 16 rows; P in the score accumulators (bf16-rounded).
-template <int HD, int KB>
-__device__ __forceinline__ void pv_accum(float (&o)[HD / 8][4], const float (&p)[KB / 8][4], const bf16* V,
-                                         int lane) {
-  constexpr int LD = HD + 8;
-  const int j = lane >> 3;
-#pragma unroll
-  for (int kt = 0; kt < KB / 16; ++kt) {
-    uint32_t pa[4] = {pack_bf16(p[2 * kt][0], p[2 * kt][1]), pack_bf16(p[2 * kt][2], p[2 * kt][3]),
-                      pack_bf16(p[2 * kt + 1][0], p[2 * kt + 1][1]), pack_bf16(p[2 * kt + 1][2], p[2 * kt + 1][3])};
-#pragma unroll
-    for (int d2 = 0; d2 < HD / 16; ++d2) {
-      uint32_t vf[4];
-      ldsm_x4_t(vf, V + (kt * 16 + (j & 1) * 8 + (lane & 7)) * LD + d2 * 16 + (j >> 1) * 8);
-      mma16816(o[2 * d2], pa, vf[0], vf[1]);
-      mma16816(o[2 * d2 + 1], pa, vf[2], vf[3]);
-    }
-  }
-}
-
-// The same two products with K and V tiles written by TMA: per 64-dim half a
-// [64 keys][128 bytes] tile with 128-byte swizzling (16-byte chunk c of key
-// row k stored at chunk c ^ (k & 7)).
-__device__ __forceinline__ const unsigned char* sw_addr(const unsigned char* tile, int row, int chunk) {
-  return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
-template <int HD>
-__device__ __forceinline__ void qk_scores_sw(float (&sc)[kKB / 8][4], const uint32_t (&qf)[HD / 16][4],
-                                             const unsigned char* K, int lane) {
-#pragma unroll
-  for (int nt = 0; nt < kKB / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-  const int j = lane >> 3;
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-    const unsigned char* tile = K + (kk >> 2) * (kKB * 128);
-#pragma unroll
-    for (int n2 = 0; n2 < kKB / 16; ++n2) {
-      uint32_t kf[4];
-      ldsm_x4(kf, sw_addr(tile, n2 * 16 + (j >> 1) * 8 + (lane & 7), (kk & 3) * 2 + (j & 1)));
-      mma16816(sc[2 * n2], qf[kk], kf[0], kf[1]);
-      mma16816(sc[2 * n2 + 1], qf[kk], kf[2], kf[3]);
-    }
-  }
-}
-
-template <int HD>
-__device__ __forceinline__ void pv_accum_sw(float (&o)[HD / 8][4], const float (&p)[kKB / 8][4],
-                                            const unsigned char* V, int lane) {
-  const int j = lane >> 3;
-#pragma unroll
-  for (int kt = 0; kt < kKB / 16; ++kt) {
-    uint32_t pa[4] = {pack_bf16(p[2 * kt][0], p[2 * kt][1]), pack_bf16(p[2 * kt][2], p[2 * kt][3]),
-                      pack_bf16(p[2 * kt + 1][0], p[2 * kt + 1][1]), pack_bf16(p[2 * kt + 1][2], p[2 * kt + 1][3])};
-#pragma unroll
-    for (int d2 = 0; d2 < HD / 16; ++d2) {
-      uint32_t vf[4];
-      ldsm_x4_t(vf, sw_addr(V + (d2 >> 2) * (kKB * 128), kt * 16 + (j & 1) * 8 + (lane & 7), (d2 & 3) * 2 + (j >> 1)));
-      mma16816(o[2 * d2], pa, vf[0], vf[1]);
-      mma16816(o[2 * d2 + 1], pa, vf[2], vf[3]);
-    }
-  }
-}
-
-template <int HD>
-__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[HD / 16][4], const bf16* Q, int warp, int lane) {
-  constexpr int LD = HD + 8;
-  const int j = lane >> 3;
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk)
-    ldsm_x4(qf[kk], Q + (warp * 16 + (j & 1) * 8 + (lane & 7)) * LD + kk * 16 + (j >> 1) * 8);
-}
-
-// Prefix partials: CTA = (64 query vectors of one request and KV head, one
-// split of the prefix).  Query vector v of the request is recompute slot
-// off_r + v / G, query head kvh * G + v % G.  K/V blocks of 64 keys stream
-// through a STAGES-deep ring of TMA loads (one (64-dim, 1-head, 64-key) box
-// per 64-dim half); the split CTAs of a query tile form one cluster (along z):
-// after their streaming loops every CTA sends its partial state (max,
-// denominator, unnormalised output) of each query row to the CTA that owns
-// the row, and each owner merges the S states in rank order and writes one
-// merged state per query.
-template <int HD, int STAGES>
-constexpr int prefix_smem_bytes() {
-  return STAGES * 2 * (HD / 64) * (kKB * 128) + kQT * (HD + 8) * 2 + 64 + 1024;
-}
-
-template <int HD, int STAGES>
-__global__ void __launch_bounds__(128) attn_prefix_mma(const __grid_constant__ CUtensorMap tmK,
-                                                       const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
-  constexpr int LD = HD + 8;
-  constexpr int XLD = HD + 2;  // exchange row: o[HD], m, l
-  constexpr int KTILE = kKB * 128;
-  constexpr int STAGE = 2 * (HD / 64) * KTILE;
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  unsigned char* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  bf16* sQ = reinterpret_cast<bf16*>(base + STAGES * STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * STAGE + kQT * LD * 2);
-  float* xbuf = reinterpret_cast<float*>(base);  // exchange area, reused after the loop
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // grid: x = (request, KV head), y = query tile, z = split; the first query
-  // tiles of every (request, KV head) are dispatched first, and the tiles that
-  // only a larger recompute set would fill come last
-  const int r = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
-  const Splits sp = fixed_splits(a.P);
-  const int G = a.nq / a.nkv;
-  // Every kernel of the pass lets its dependants start only after its own
-  // dependency wait, so the kernels before the previous one have completed
-  // when this grid starts: the recompute offsets (gate kernel) can be read
-  // before the wait, past L1.  Only the queries (previous kernel) wait.
-  const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
-  const int q0 = blockIdx.y * kQT;
-  // An empty tile leaves without the dependency wait: it reads nothing of the
-  // previous kernel, and the live tiles (the main branch always recomputes,
-  // so there is one per request and KV head) still hold the next kernel back
-  // until they have waited.  Uniform over the cluster.
-  if (q0 >= nqv) return;
-  const int s = sp.S > 1 ? (int)cluster_rank() : 0;
-  const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
-  const int nblk = k_hi > k_lo ? (k_hi - k_lo + kKB - 1) / kKB : 0;
-  const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
-
-  if (tid == 0) {
-    for (int st = 0; st < STAGES; ++st) tc::mbar_init(&full[st], 1);
-    tc::fence_barrier_init();
-  }
-  __syncthreads();
-  auto issue = [&](int b) {  // thread 0: K and V of key block b into its stage
-    const int st = b % STAGES;
-    unsigned char* sk = base + st * STAGE;
-    const int z = r * a.P + k_lo + b * kKB;
-    tc::mbar_expect_tx(&full[st], STAGE);
-#pragma unroll
-    for (int h = 0; h < HD / 64; ++h) {
-      tc::tma_load_3d(sk + h * KTILE, &tmK, h * 64, kvh, z, &full[st]);
-      tc::tma_load_3d(sk + (HD / 64 + h) * KTILE, &tmV, h * 64, kvh, z, &full[st]);
-    }
-  };
-  // the prefix keys and values are inputs of the pass: every stage is filled
-  // before the wait (with P <= 1024 that is the whole split)
-  if (tid == 0)
-    for (int b = 0; b < min(STAGES, nblk); ++b) issue(b);
-  pdl_wait();
-  pdl_trigger();
-
-  for (int idx = tid; idx < kQT * (HD / 8); idx += 128) {
-    const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
-    const bool ok = v < nqv;
-    const int g = off_r + (ok ? v / G : 0), h = kvh * G + (ok ? v % G : 0);
-    cp_async16(sQ + row * LD + c8 * 8, qkv + (size_t)g * a.ld_qkv + h * HD + c8 * 8, ok);
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  uint32_t qf[HD / 16][4];
-  load_q_frags<HD>(qf, sQ, warp, lane);
-
-  float o[HD / 8][4];
-#pragma unroll
-  for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  for (int b = 0; b < nblk; ++b) {
-    // block b + STAGES - 1 goes to the stage the last barrier freed (the
-    // first STAGES blocks were issued before the wait)
-    if (tid == 0 && b >= 1 && b + STAGES - 1 < nblk) issue(b + STAGES - 1);
-    // a wait that gives up raises the error word but does not leave the loop,
-    // so every warp keeps reaching the same barriers
-    tc::mbar_wait(&full[b % STAGES], (b / STAGES) & 1, a.err);
-    const unsigned char* sk = base + (b % STAGES) * STAGE;
-    float sc[kKB / 8][4];
-    qk_scores_sw<HD>(sc, qf, sk, lane);
-    const int kb0 = k_lo + b * kKB;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < kKB / 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = kb0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-        sc[nt][e] = key < k_hi ? sc[nt][e] * a.scale_log2 : -INFINITY;
-      }
-      mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-    }
-    const float n0 = fmaxf(m0, quad_max(mx0)), n1 = fmaxf(m1, quad_max(mx1));
-    const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < kKB / 8; ++nt) {
-      sc[nt][0] = exp2f(sc[nt][0] - n0);
-      sc[nt][1] = exp2f(sc[nt][1] - n0);
-      sc[nt][2] = exp2f(sc[nt][2] - n1);
-      sc[nt][3] = exp2f(sc[nt][3] - n1);
-      s0 += sc[nt][0] + sc[nt][1];
-      s1 += sc[nt][2] + sc[nt][3];
-    }
-    l0 = l0 * c0 + s0;
-    l1 = l1 * c1 + s1;
-    m0 = n0;
-    m1 = n1;
-#pragma unroll
-    for (int nt = 0; nt < HD / 8; ++nt) {
-      o[nt][0] *= c0;
-      o[nt][1] *= c0;
-      o[nt][2] *= c1;
-      o[nt][3] *= c1;
-    }
-    pv_accum_sw<HD>(o, sc, sk + (HD / 64) * KTILE, lane);
-    __syncthreads();
-  }
-  l0 = quad_sum(l0);
-  l1 = quad_sum(l1);
-
-  if (sp.S == 1) {  // a single split: the partial is already the merged state
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
-      if (v >= nqv) continue;
-      const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
-      float* po = a.part_o + qi * HD + (lane & 3) * 2;
-#pragma unroll
-      for (int nt = 0; nt < HD / 8; ++nt)
-        *reinterpret_cast<float2*>(po + nt * 8) = make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-      if ((lane & 3) == 0) {
-        a.part_ml[qi * 2 + 0] = half ? m1 : m0;
-        a.part_ml[qi * 2 + 1] = half ? l1 : l0;
-      }
-    }
-    return;
-  }
-  // rows [rank * per, (rank + 1) * per) of the tile are merged by `rank`
-  const int per = (kQT + sp.S - 1) / sp.S;
-  cluster_sync_all();  // every CTA is past its loop: exchange areas are free
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int vr = warp * 16 + (lane >> 2) + half * 8;  // row within the tile
-    const int owner = vr / per;
-    const uint32_t dst = map_rank(smem_addr(xbuf + ((size_t)s * per + (vr - owner * per)) * XLD), (uint32_t)owner);
-#pragma unroll
-    for (int nt = 0; nt < HD / 8; ++nt)
-      st_cluster_v2(dst + (nt * 8 + (lane & 3) * 2) * 4, o[nt][2 * half], o[nt][2 * half + 1]);
-    if ((lane & 3) == 0) {
-      st_cluster_f32(dst + HD * 4, half ? m1 : m0);
-      st_cluster_f32(dst + (HD + 1) * 4, half ? l1 : l0);
-    }
-  }
-  cluster_sync_all();  // every partial has arrived
-  // one warp per merged row: the split weights are formed once per row, each
-  // lane combines features lane + 32c
-  const int rows = min(per, kQT - s * per);
-  for (int rl = warp; rl < rows; rl += 4) {
-    const int v = q0 + s * per + rl;
-    if (v >= nqv) break;
-    float mt[kMaxSplits], w[kMaxSplits];
-    float M = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < kMaxSplits; ++t) {
-      mt[t] = t < sp.S ? xbuf[((size_t)t * per + rl) * XLD + HD] : -INFINITY;
-      M = fmaxf(M, mt[t]);
-    }
-    float l = 0.f;
-#pragma unroll
-    for (int t = 0; t < kMaxSplits; ++t) {
-      w[t] = t < sp.S ? exp2f(mt[t] - M) : 0.f;
-      if (t < sp.S) l += w[t] * xbuf[((size_t)t * per + rl) * XLD + HD + 1];
-    }
-    const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
-#pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      const int dd = lane + 32 * c;
-      float acc = 0.f;
-#pragma unroll
-      for (int t = 0; t < kMaxSplits; ++t)
-        if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * XLD + dd];
-      a.part_o[qi * HD + dd] = acc;
-    }
-    if (lane == 0) {
-      a.part_ml[qi * 2 + 0] = M;
-      a.part_ml[qi * 2 + 1] = l;
-    }
-  }
-}
 
 // ------------------------------------------------------------ tcgen05 prefix path
 //
@@ -497,23 +130,45 @@ inline Splits tc_splits(int P, int groups, int target_ctas) {
   return tc_split_len(P, S);
 }
 
-template <int HD>
+// Fused kernel (short prefixes): every query tile is live, so S is the split
+// count that brings the grid to about one wave, with at least two 64-key
+// blocks a split.
+constexpr double kFusedMaxFlops = 6.0e9;
+inline Splits fused_splits(int P, int ctas, int target_ctas) {
+  int S = target_ctas / (ctas > 0 ? ctas : 1);
+  const int by_len = P / (2 * kKB);
+  S = S > by_len ? by_len : S;
+  S = S < 1 ? 1 : (S > kTcMaxSplits ? kTcMaxSplits : S);
+  return tc_split_len(P, S);
+}
+
+template <int HD, int STAGES = kTcStages>
 struct TcLayout {
+  static constexpr int ST = STAGES;                     // K (and V) ring stages
   static constexpr int QH = HD / 64;                    // 64-dim halves
   static constexpr int HALF = kTcQ * 128;               // one 64-dim half of Q: 128 rows x 128 B
   static constexpr int KV_TILE = kKB * 128;             // one 64-dim half of a K or V block
   static constexpr int STAGE = QH * KV_TILE;            // K (or V) of one block
   static constexpr int P_TILE = kTcQ * 128;             // P: 128 rows x 64 keys (bf16)
   static constexpr int OFF_K = QH * HALF;
-  static constexpr int OFF_V = OFF_K + kTcStages * STAGE;
-  static constexpr int OFF_P = OFF_V + kTcStages * STAGE;
+  static constexpr int OFF_V = OFF_K + ST * STAGE;
+  static constexpr int OFF_P = OFF_V + ST * STAGE;
   static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
   static constexpr int BYTES = OFF_BAR + 256 + 1024;   // + alignment of the dynamic window
+  // fused variant: the branch's own block keys and values (one 64-key block,
+  // gathered), after the barriers; 128-byte-swizzled tiles start on a
+  // 1024-byte boundary, where the MMA descriptors place the swizzle atoms
+  static constexpr int OFF_BK = (OFF_BAR + 256 + 1023) / 1024 * 1024;
+  static constexpr int OFF_BV = OFF_BK + STAGE;
+  static constexpr int BYTES_FUSED = OFF_BV + STAGE + 1024;
   static constexpr int XLD = HD + 4;                    // merge exchange row: o[HD], m, l (16-byte rows)
   static constexpr int SBUF = 3;                        // score buffers: columns [64 s, 64 s + 64)
   static constexpr int O_COL = 256;                     // O: columns [256, 256 + HD)
   static constexpr int TMEM_COLS = 512;
   static_assert((kTcQ + kMaxSplits - 1) * XLD * 4 <= OFF_P, "merge exchange area");
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && OFF_BK % 1024 == 0 &&
+                    OFF_BV % 1024 == 0,
+                "swizzled tiles on 1024-byte boundaries");
 };
 
 __device__ __forceinline__ void tmem_ld32_raw(uint32_t taddr, float (&v)[32]) { tc::tmem_ld32(taddr, v); }
@@ -525,11 +180,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-template <int HD>
+// kFused: the whole attention of every row of a branch in one kernel, for
+// short prefixes.  The CTA's 128 query vectors are rows of one branch (row
+// (b, v / G), query head kvh * G + v % G, the query of the row's source), the
+// last split appends the branch's own block keys and values as one more
+// 64-key block (gathered like Q, zero past L), and the merged state is
+// normalised and written as the attention output: no partial state and no
+// block kernel.  Folded rows repeat their source's prefix scores, which costs
+// little while the prefix is short.
+template <int HD, bool kFused>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_constant__ CUtensorMap tmK,
                                                                 const __grid_constant__ CUtensorMap tmV,
                                                                 const AttnArgs a) {
-  using Lay = TcLayout<HD>;
+  // the fused variant keeps three K/V stages, which leaves room for the
+  // branch's block keys and values
+  using Lay = TcLayout<HD, kFused ? 3 : kTcStages>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -538,11 +203,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   unsigned char* sV = base + Lay::OFF_V;
   unsigned char* sP = base + Lay::OFF_P;
   uint64_t* bar = reinterpret_cast<uint64_t*>(base + Lay::OFF_BAR);
-  uint64_t* kfull = bar;                   // [kTcStages] K landed
-  uint64_t* vfull = bar + kTcStages;       // [kTcStages] V landed
-  uint64_t* kempty = bar + 2 * kTcStages;  // [kTcStages] K consumed by S = Q K^T
-  uint64_t* vempty = bar + 3 * kTcStages;  // [kTcStages] V consumed by O += P V
-  uint64_t* sfull = bar + 4 * kTcStages;   // [SBUF] scores in TMEM
+  uint64_t* kfull = bar;                   // [Lay::ST] K landed
+  uint64_t* vfull = bar + Lay::ST;       // [Lay::ST] V landed
+  uint64_t* kempty = bar + 2 * Lay::ST;  // [Lay::ST] K consumed by S = Q K^T
+  uint64_t* vempty = bar + 3 * Lay::ST;  // [Lay::ST] V consumed by O += P V
+  uint64_t* sfull = bar + 4 * Lay::ST;   // [SBUF] scores in TMEM
   uint64_t* sempty = sfull + Lay::SBUF;    // [SBUF] scores read
   uint64_t* pfull = sempty + Lay::SBUF;    // [2] P written
   uint64_t* pvdone = pfull + 2;            // [2] P V of that buffer done
@@ -553,14 +218,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   __shared__ float xmax[2][2][kTcQ];             // [block parity][half][row]: partial block maxima
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // grid: x = (request, KV head), y = query tile, z = split; the first query
-  // tiles of every (request, KV head) are dispatched first, and the tiles that
-  // only a larger recompute set would fill come last
-  const int r = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
+  // grid: x = (request, KV head) -- fused: (branch, KV head) --, y = query
+  // tile, z = split; the first query tiles of every x are dispatched first,
+  // and the tiles that only a larger recompute set would fill come last
+  const int xr = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
+  const int r = kFused ? xr / a.Bp : xr;
   const Splits sp = tc_split_len(a.P, (int)gridDim.z);
   const int G = a.nq / a.nkv;
   // recompute offsets from the gate kernel (complete once this grid runs), past L1
-  const int off_r = __ldcg(a.meta + 1 + r), nqv = (__ldcg(a.meta + 2 + r) - off_r) * G;
+  const int off_r = kFused ? 0 : __ldcg(a.meta + 1 + r);
+  const int nqv = kFused ? a.L * G : (__ldcg(a.meta + 2 + r) - off_r) * G;
   const int q0 = blockIdx.y * kTcQ;
   // An empty tile leaves without the dependency wait: it reads nothing of the
   // previous kernel, and the live tiles (the main branch always recomputes,
@@ -569,10 +236,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   if (q0 >= nqv) return;
   const int s = sp.S > 1 ? (int)tc::cluster_ctarank() : 0;
   const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
-  const int nblk = (k_hi - k_lo + kKB - 1) / kKB;
+  const int nblk_p = (k_hi - k_lo + kKB - 1) / kKB;  // prefix blocks of this split
+  // fused: the last split takes the branch's block keys as one more block
+  const bool with_block = kFused && s == sp.S - 1;
+  const int nblk = nblk_p + (with_block ? 1 : 0);
 
   if (tid == 0) {
-    for (int i = 0; i < kTcStages; ++i) {
+    for (int i = 0; i < Lay::ST; ++i) {
       tc::mbar_init(&kfull[i], 1);
       tc::mbar_init(&vfull[i], 1);
       tc::mbar_init(&kempty[i], 1);
@@ -596,10 +266,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // warp 0: lane 0 loads key block b into K stage b % kTcStages, lane 1 the
+  // warp 0: lane 0 loads key block b into K stage b % Lay::ST, lane 1 the
   // value block into the V ring
   auto issue = [&](int b, bool keys) {
-    const int st = b % kTcStages;
+    const int st = b % Lay::ST;
     unsigned char* dst = (keys ? sK : sV) + st * Lay::STAGE;
     uint64_t* full = keys ? &kfull[st] : &vfull[st];
     const int z = r * a.P + k_lo + b * kKB;
@@ -609,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   };
   // the prefix keys and values are inputs of the pass
   if (warp == 0 && lane < 2)
-    for (int b = 0; b < min(kTcStages, nblk); ++b) issue(b, lane == 0);
+    for (int b = 0; b < min(Lay::ST, nblk_p); ++b) issue(b, lane == 0);
   pdl_wait();
   pdl_trigger();
 
@@ -617,9 +287,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   if (warp == 0) {
     if (lane < 2) {
       const bool keys = lane == 0;
-      for (int b = kTcStages; b < nblk; ++b) {
-        // the stage is free once the MMA that read block b - kTcStages has completed
-        tc::mbar_wait(keys ? &kempty[b % kTcStages] : &vempty[b % kTcStages], ((b / kTcStages) - 1) & 1, a.err);
+      for (int b = Lay::ST; b < nblk_p; ++b) {
+        // the stage is free once the MMA that read block b - Lay::ST has completed
+        tc::mbar_wait(keys ? &kempty[b % Lay::ST] : &vempty[b % Lay::ST], ((b / Lay::ST) - 1) & 1, a.err);
         issue(b, keys);
       }
     }
@@ -630,11 +300,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       const uint32_t idesc_pv = tc::idesc_bf16_f32(kTcQ, HD) | (1u << 16);  // V is MN-major
       tc::mbar_wait(qready, 0, a.err);
       auto issue_s = [&](int b) {  // S(b) = Q K(b)^T into score buffer b % SBUF
-        const int st = b % kTcStages, sb = b % Lay::SBUF;
-        tc::mbar_wait(&kfull[st], (b / kTcStages) & 1, a.err);
+        const int st = b % Lay::ST, sb = b % Lay::SBUF;
+        const bool blk = b >= nblk_p;  // fused: the branch's block keys, ready with Q
+        if (!blk) tc::mbar_wait(&kfull[st], (b / Lay::ST) & 1, a.err);
         if (b >= Lay::SBUF) tc::mbar_wait(&sempty[sb], ((b / Lay::SBUF) - 1) & 1, a.err);
         tc::fence_after_sync();
-        const unsigned char* sk = sK + st * Lay::STAGE;
+        const unsigned char* sk = blk ? base + Lay::OFF_BK : sK + st * Lay::STAGE;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint64_t dq = tc::sw128_kmajor_desc(smem_addr(sQ + (kk >> 2) * Lay::HALF + (kk & 3) * 32));
@@ -642,18 +313,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
           tc::mma_bf16(tmem + sb * kKB, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&sfull[sb]);
-        tc::mma_commit(&kempty[st]);
+        if (!blk) tc::mma_commit(&kempty[st]);
       };
       for (int b = 0; b < min(Lay::SBUF - 1, nblk); ++b) issue_s(b);
       for (int j = 0; j < nblk; ++j) {
         // the scores SBUF - 1 blocks ahead, as soon as their buffer is read
         if (j + Lay::SBUF - 1 < nblk) issue_s(j + Lay::SBUF - 1);
         // O += P(j) V(j)
-        const int st = j % kTcStages, pb = j & 1;
+        const int st = j % Lay::ST, pb = j & 1;
+        const bool blk = j >= nblk_p;
         tc::mbar_wait(&pfull[pb], (j >> 1) & 1, a.err);
-        tc::mbar_wait(&vfull[st], (j / kTcStages) & 1, a.err);
+        if (!blk) tc::mbar_wait(&vfull[st], (j / Lay::ST) & 1, a.err);
         tc::fence_after_sync();
-        const unsigned char* sv = sV + st * Lay::STAGE;
+        const unsigned char* sv = blk ? base + Lay::OFF_BV : sV + st * Lay::STAGE;
 #pragma unroll
         for (int kk = 0; kk < kKB / 16; ++kk) {
           const uint64_t dp = tc::sw128_kmajor_desc(smem_addr(sP + pb * Lay::P_TILE + kk * 32));
@@ -661,7 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
           tc::mma_bf16(tmem + Lay::O_COL, dp, dv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc::mma_commit(&pvdone[pb]);
-        tc::mma_commit(&vempty[st]);
+        if (!blk) tc::mma_commit(&vempty[st]);
       }
       tc::mma_commit(ofull);
     }
@@ -676,11 +348,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
     const int v = q0 + row;
     {
       const bool ok = v < nqv;
-      const int g = off_r + (ok ? v / G : 0), h = kvh * G + (ok ? v % G : 0);
+      // fused: row (b, v / G) of the branch, whose query is its source's
+      const int g = kFused ? __ldcg(a.rcslot + xr * a.L + (ok ? v / G : 0)) : off_r + (ok ? v / G : 0);
+      const int h = kvh * G + (ok ? v % G : 0);
       const bf16* src = qkv + (size_t)g * a.ld_qkv + h * HD;
 #pragma unroll
       for (int c = half * (HD / 16); c < (half + 1) * (HD / 16); ++c)
         cp_async16(sQ + (c >> 3) * Lay::HALF + row * 128 + (((c & 7) ^ (row & 7)) << 4), src + c * 8, ok);
+      if (kFused && with_block) {
+        // the branch's block keys and values: key m of the branch's table is
+        // the K/V row of its source slot (zero past L); 256 threads, 64 keys
+        const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
+        const int t = tid - 64;
+        for (int idx = t; idx < kKB * (HD / 8); idx += 256) {
+          const int m = idx / (HD / 8), c = idx % (HD / 8);
+          const int gm = m < a.L ? __ldcg(a.rcslot + xr * a.L + m) : 0;
+          const bf16* kr = qkv + (size_t)gm * a.ld_qkv;
+          const int off = (c >> 3) * Lay::KV_TILE + m * 128 + (((c & 7) ^ (m & 7)) << 4);
+          cp_async16(base + Lay::OFF_BK + off, kr + koff + c * 8, m < a.L);
+          cp_async16(base + Lay::OFF_BV + off, kr + voff + c * 8, m < a.L);
+        }
+      }
       cp_async_commit();
       cp_async_wait<0>();
       tc::fence_proxy_async_smem();
@@ -697,11 +385,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       tmem_ld32_raw(tl + sb * kKB + 32 * half, sc);
       tc::fence_before_sync();
       tc::mbar_arrive(&sempty[sb]);
-      const int kb0 = k_lo + b * kKB + 32 * half;
-      if (kb0 + 32 > k_hi) {  // the split's last block may be ragged
+      if (kFused && b >= nblk_p) {  // the branch's block keys: 64 slots, L of them real
+        const int m0 = 32 * half;
+        if (m0 + 32 > a.L) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (kb0 + k >= k_hi) sc[k] = -INFINITY;
+          for (int k = 0; k < 32; ++k)
+            if (m0 + k >= a.L) sc[k] = -INFINITY;
+        }
+      } else {
+        const int kb0 = k_lo + b * kKB + 32 * half;
+        if (kb0 + 32 > k_hi) {  // the split's last block may be ragged
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (kb0 + k >= k_hi) sc[k] = -INFINITY;
+        }
       }
       float mx = sc[0];
 #pragma unroll
@@ -769,13 +466,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       tmem_ld32_raw(tl + Lay::O_COL + half * HO + c0, *reinterpret_cast<float(*)[32]>(o + c0));
     if (sp.S == 1) {  // a single split: the partial is already the merged state
       if (v < nqv) {
-        const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
-        float* po = a.part_o + qi * HD + half * HO;
+        if constexpr (kFused) {
+          const float inv = 1.f / lrow;
+          bf16* dst = reinterpret_cast<bf16*>(a.attn) + (size_t)(xr * a.L + v / G) * a.ld_attn +
+                      (kvh * G + v % G) * HD + half * HO;
 #pragma unroll
-        for (int c = 0; c < HO; c += 4) *reinterpret_cast<float4*>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        if (half == 0) {
-          a.part_ml[qi * 2 + 0] = mrow;
-          a.part_ml[qi * 2 + 1] = lrow;
+          for (int c = 0; c < HO; c += 8)
+            *reinterpret_cast<uint4*>(dst + c) =
+                make_uint4(pack_bf16(o[c] * inv, o[c + 1] * inv), pack_bf16(o[c + 2] * inv, o[c + 3] * inv),
+                           pack_bf16(o[c + 4] * inv, o[c + 5] * inv), pack_bf16(o[c + 6] * inv, o[c + 7] * inv));
+        } else {
+          const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+          float* po = a.part_o + qi * HD + half * HO;
+#pragma unroll
+          for (int c = 0; c < HO; c += 4)
+            *reinterpret_cast<float4*>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+          if (half == 0) {
+            a.part_ml[qi * 2 + 0] = mrow;
+            a.part_ml[qi * 2 + 1] = lrow;
+          }
         }
       }
     } else {
@@ -818,19 +527,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
         w[t] = t < sp.S ? exp2f(mt[t] - M) : 0.f;
         if (t < sp.S) lsum += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + HD + 1];
       }
-      const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+      if constexpr (kFused) {
+        const float inv = 1.f / lsum;
+        bf16* dst = reinterpret_cast<bf16*>(a.attn) + (size_t)(xr * a.L + v / G) * a.ld_attn + (kvh * G + v % G) * HD;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        const int dd = lane + 32 * c;
-        float acc = 0.f;
+        for (int c = 0; c < HD / 32; ++c) {
+          const int dd = lane + 32 * c;
+          float acc = 0.f;
 #pragma unroll
-        for (int t = 0; t < kMaxSplits; ++t)
-          if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + dd];
-        a.part_o[qi * HD + dd] = acc;
-      }
-      if (lane == 0) {
-        a.part_ml[qi * 2 + 0] = M;
-        a.part_ml[qi * 2 + 1] = lsum;
+          for (int t = 0; t < kMaxSplits; ++t)
+            if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + dd];
+          dst[dd] = __float2bfloat16_rn(acc * inv);
+        }
+      } else {
+        const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          const int dd = lane + 32 * c;
+          float acc = 0.f;
+#pragma unroll
+          for (int t = 0; t < kMaxSplits; ++t)
+            if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + dd];
+          a.part_o[qi * HD + dd] = acc;
+        }
+        if (lane == 0) {
+          a.part_ml[qi * 2 + 0] = M;
+          a.part_ml[qi * 2 + 1] = lsum;
+        }
       }
     }
   }
@@ -839,151 +562,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, Lay::TMEM_COLS);
-  }
-}
-
-// Block attention + merge: CTA = (32 query vectors of one branch and KV head,
-// two warps).  Query vector v is block position n = v / G with query head
-// kvh * G + v % G; its query is the one of the row's resolved source; its
-// block keys/values are the branch's own table K_i[m] = QKV[rcslot(i, m)].
-constexpr int kBQT = 32;
-
-template <int HD, int KB>
-__global__ void __launch_bounds__(64) attn_block_mma(const AttnArgs a) {
-  constexpr int LD = HD + 8;
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int slot[KB];
-  bf16* sQ = reinterpret_cast<bf16*>(smem);
-  bf16* sK = sQ + kBQT * LD;
-  bf16* sV = sK + KB * LD;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rb = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;  // rb = r * Bp + i
-  const int G = a.nq / a.nkv, L = a.L;
-  const int q0 = blockIdx.x * kBQT, nqv = L * G;
-  if (q0 >= nqv) {
-    pdl_wait();
-    return;
-  }
-  // Every kernel of the pass lets its dependants start only after its own
-  // dependency wait, so the kernels before the previous one have completed
-  // when this grid starts: the source slots (gate kernel) are read before the
-  // wait, past L1, and so are the projected rows when the prefix kernel sits
-  // between the projection and this one.
-  const int count = __ldcg(a.meta);
-  const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
-  const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
-  for (int m = tid; m < KB; m += 64) {
-    int g = m < L ? __ldcg(a.rcslot + rb * L + m) : 0;
-    if (g < 0 || g >= count) {
-      raise_error(a.err, kErrAttn);
-      g = 0;
-    }
-    slot[m] = g;
-  }
-  __syncthreads();
-  auto load_rows = [&] {
-    for (int idx = tid; idx < kBQT * (HD / 8); idx += 64) {
-      const int row = idx / (HD / 8), c8 = idx % (HD / 8), v = q0 + row;
-      const bool ok = v < nqv;
-      cp_async16(sQ + row * LD + c8 * 8,
-                 qkv + (size_t)slot[ok ? v / G : 0] * a.ld_qkv + (kvh * G + (ok ? v % G : 0)) * HD + c8 * 8, ok);
-    }
-    for (int idx = tid; idx < KB * (HD / 8); idx += 64) {
-      const int m = idx / (HD / 8), c8 = idx % (HD / 8);
-      const bf16* src = qkv + (size_t)slot[m] * a.ld_qkv;
-      cp_async16(sK + m * LD + c8 * 8, src + koff + c8 * 8, m < L);
-      cp_async16(sV + m * LD + c8 * 8, src + voff + c8 * 8, m < L);
-    }
-    cp_async_commit();
-  };
-  if (a.P > 0) load_rows();
-  pdl_wait();
-  pdl_trigger();
-  if (a.P == 0) load_rows();
-  // the merged prefix state of this thread's two query vectors (previous
-  // kernel), needed only after the block part: loaded into registers while it
-  // runs
-  float mp[2] = {0.f, 0.f}, lp[2] = {0.f, 0.f};
-  float2 pp[2][HD / 8];
-  if (a.P > 0) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
-      const size_t qi = v < nqv ? (size_t)slot[v / G] * a.nq + kvh * G + v % G : (size_t)slot[0] * a.nq + kvh * G;
-      const float* po = a.part_o + qi * HD + (lane & 3) * 2;
-#pragma unroll
-      for (int nt = 0; nt < HD / 8; ++nt) pp[half][nt] = *reinterpret_cast<const float2*>(po + nt * 8);
-      mp[half] = a.part_ml[qi * 2];
-      lp[half] = a.part_ml[qi * 2 + 1];
-    }
-  }
-  cp_async_wait<0>();  // the projected rows have landed
-  __syncthreads();
-  uint32_t qf[HD / 16][4];
-  load_q_frags<HD>(qf, sQ, warp, lane);
-  float sc[KB / 8][4];
-  qk_scores<HD, KB>(sc, qf, sK, lane);
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < KB / 8; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int m = nt * 8 + (lane & 3) * 2 + (e & 1);
-      sc[nt][e] = m < L ? sc[nt][e] * a.scale_log2 : -INFINITY;
-    }
-    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-  }
-  const float mb0 = quad_max(mx0), mb1 = quad_max(mx1);
-  float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < KB / 8; ++nt) {
-    sc[nt][0] = exp2f(sc[nt][0] - mb0);
-    sc[nt][1] = exp2f(sc[nt][1] - mb0);
-    sc[nt][2] = exp2f(sc[nt][2] - mb1);
-    sc[nt][3] = exp2f(sc[nt][3] - mb1);
-    s0 += sc[nt][0] + sc[nt][1];
-    s1 += sc[nt][2] + sc[nt][3];
-  }
-  const float lb0 = quad_sum(s0), lb1 = quad_sum(s1);
-  float o[HD / 8][4];
-#pragma unroll
-  for (int nt = 0; nt < HD / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  pv_accum<HD, KB>(o, sc, sV, lane);
-
-  bf16* out = reinterpret_cast<bf16*>(a.attn);
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int v = q0 + warp * 16 + (lane >> 2) + half * 8;
-    if (v >= nqv) continue;
-    const int row = rb * L + v / G, h = kvh * G + v % G;
-    const float mb = half ? mb1 : mb0, lb = half ? lb1 : lb0;
-    float acc[HD / 8][2];
-    float l, wb;
-    if (a.P > 0) {
-      // merge with the prefix state of this query (one per recompute slot and head)
-      const float M = fmaxf(mb, mp[half]);
-      wb = exp2f(mb - M);
-      const float wp = exp2f(mp[half] - M);
-      l = lb * wb + lp[half] * wp;
-#pragma unroll
-      for (int nt = 0; nt < HD / 8; ++nt) {
-        acc[nt][0] = o[nt][2 * half] * wb + wp * pp[half][nt].x;
-        acc[nt][1] = o[nt][2 * half + 1] * wb + wp * pp[half][nt].y;
-      }
-    } else {
-      l = lb;
-#pragma unroll
-      for (int nt = 0; nt < HD / 8; ++nt) {
-        acc[nt][0] = o[nt][2 * half];
-        acc[nt][1] = o[nt][2 * half + 1];
-      }
-    }
-    const float inv = 1.f / l;
-    bf16* dst = out + (size_t)row * a.ld_attn + h * HD + (lane & 3) * 2;
-#pragma unroll
-    for (int nt = 0; nt < HD / 8; ++nt)
-      *reinterpret_cast<__nv_bfloat162*>(dst + nt * 8) = __floats2bfloat162_rn(acc[nt][0] * inv, acc[nt][1] * inv);
   }
 }
 
@@ -1018,6 +596,7 @@ struct BlkLayout {
   static __host__ __device__ constexpr int off_v(int nk) { return off_k() + QH * kv_half(nk); }
   static __host__ __device__ constexpr int off_bar(int nk) { return off_v(nk) + QH * kv_half(nk); }
   static __host__ __device__ constexpr int bytes(int nk) { return off_bar(nk) + 64 + 1024; }
+  static_assert(QH * Q_HALF % 1024 == 0 && kv_half(32) % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
 };
 
 template <int HD>
@@ -1184,8 +763,6 @@ __global__ void __launch_bounds__(kBlkQ) attn_block_tc(const AttnArgs a) {
     l = lb * wb + lp * wp;
   }
   const float inv = 1.f / l;
-  tc::mbar_wait(&bar[1], 0, a.err);
-  tc::fence_after_sync();
   bf16* dst = reinterpret_cast<bf16*>(a.attn) + (size_t)(rb * L + vn) * a.ld_attn + (kvh * G + (live ? v % G : 0)) * HD;
   float* po = a.part_o + qi * HD;
   // correction mode: the row's merged state (max in log2 units, denominator,
@@ -1194,8 +771,22 @@ __global__ void __launch_bounds__(kBlkQ) attn_block_tc(const AttnArgs a) {
     a.part_ml[qi * 2] = a.P > 0 ? fmaxf(mb, mp) : mb;
     a.part_ml[qi * 2 + 1] = l;
   }
+  // the prefix partial is read 32 columns at a time, each chunk's loads issued
+  // before the previous chunk is applied (the first while P V runs)
+  const bool pre = a.P > 0 && live;
+  float4 cur[8], nxt[8];
+  if (pre) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) cur[e] = *reinterpret_cast<const float4*>(po + 4 * e);
+  }
+  tc::mbar_wait(&bar[1], 0, a.err);
+  tc::fence_after_sync();
 #pragma unroll
   for (int c0 = 0; c0 < HD; c0 += 32) {
+    if (pre && c0 + 32 < HD) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) nxt[e] = *reinterpret_cast<const float4*>(po + c0 + 32 + 4 * e);
+    }
     float o[32];
     tc::tmem_ld32(tl + c0, o);
     if (live) {
@@ -1205,8 +796,7 @@ __global__ void __launch_bounds__(kBlkQ) attn_block_tc(const AttnArgs a) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = o[c + e] * wb;
         if (a.P > 0) {
-          const float4 p0 = *reinterpret_cast<const float4*>(po + c0 + c);
-          const float4 p1 = *reinterpret_cast<const float4*>(po + c0 + c + 4);
+          const float4 p0 = cur[c / 4], p1 = cur[c / 4 + 1];
           x[0] += wp * p0.x; x[1] += wp * p0.y; x[2] += wp * p0.z; x[3] += wp * p0.w;
           x[4] += wp * p1.x; x[5] += wp * p1.y; x[6] += wp * p1.z; x[7] += wp * p1.w;
         }
@@ -1219,6 +809,8 @@ __global__ void __launch_bounds__(kBlkQ) attn_block_tc(const AttnArgs a) {
         }
       }
     }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) cur[e] = nxt[e];
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1461,53 +1053,48 @@ __global__ void __launch_bounds__(128) attn_correct_kernel(const AttnArgs a) {
 }
 
 template <int HD>
-cudaError_t attention_mma(Launch& lc, const AttnArgs& a) {
-  constexpr int LD = HD + 8;
+cudaError_t attention_tc(Launch& lc, const AttnArgs& a) {
   const int G = a.nq / a.nkv;
-  // block keys per CTA tile: 32 when the block length allows, else 64
-  const int kb = a.L <= 32 ? 32 : kKB;
-  const size_t smem_b = (size_t)(kBQT + 2 * kb) * LD * sizeof(bf16);
   static cudaError_t attr = [&] {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcLayout<HD>::BYTES);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_prefix_mma<HD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               prefix_smem_bytes<HD, 2>());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_prefix_mma<HD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               prefix_smem_bytes<HD, 4>());
+      e = cudaFuncSetAttribute(attn_prefix_tc<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               TcLayout<HD, 3>::BYTES_FUSED);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, BlkLayout<HD>::bytes(64));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_block_mma<HD, kKB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)((kBQT + 2 * kKB) * LD * sizeof(bf16)));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_block_mma<HD, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)((kBQT + 2 * 32) * LD * sizeof(bf16)));
     return e;
   }();
   if (attr != cudaSuccess) return lc.err = attr;
+  // short prefixes, direct mode: one fused kernel does every row's whole
+  // attention, repeating the prefix scores of folded rows (at most about
+  // kFusedMaxFlops of score and value products for all rows of the layer)
+  const bool fused = a.P > 0 && a.mode == SF_ATTN_DIRECT &&
+                     4.0 * a.T * a.nq * a.hd * (double)a.P <= kFusedMaxFlops;
   if (a.P > 0) {
     alignas(64) CUtensorMap tmK, tmV;
     if (!make_tmap_kv(&tmK, a.pk, HD, a.nkv, (uint64_t)a.R * a.P) ||
         !make_tmap_kv(&tmV, a.pv, HD, a.nkv, (uint64_t)a.R * a.P))
       return lc.err = cudaErrorInvalidValue;
+    // fused: the whole attention of every row in the prefix kernel (short
+    // prefixes, direct mode); the grid covers every row of every branch
+    if (fused) {
+      const int tiles = (a.L * G + kTcQ - 1) / kTcQ;
+      const Splits sp = fused_splits(a.P, a.R * a.Bp * a.nkv * tiles, a.target_ctas);
+      dim3 grid(a.R * a.Bp * a.nkv, tiles, sp.S);
+      lc.before(SF_K_ATTN_PREFIX);
+      lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD, 3>::BYTES_FUSED, sp.S,
+                          attn_prefix_tc<HD, true>, tmK, tmV, a));
+      lc.after(SF_K_ATTN_PREFIX);
+      return lc.err;
+    }
     // worst case: every row of a request recomputes
     lc.before(SF_K_ATTN_PREFIX);
-    if (a.P >= kTcMinPrefix) {
+    {
       const Splits sp = tc_splits(a.P, a.R * a.nkv, a.target_ctas);
       dim3 grid(a.R * a.nkv, (a.Bp * a.L * G + kTcQ - 1) / kTcQ, sp.S);
-      lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES, sp.S, attn_prefix_tc<HD>,
+      lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES, sp.S, attn_prefix_tc<HD, false>,
                           tmK, tmV, a));
-    } else {
-      const Splits sp = fixed_splits(a.P);
-      dim3 grid(a.R * a.nkv, (a.Bp * a.L * G + kQT - 1) / kQT, sp.S);
-      if (mma_prefix_stages(a.P) == 2)
-        lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD, 2>(), sp.S, attn_prefix_mma<HD, 2>,
-                            tmK, tmV, a));
-      else
-        lc.check(launch_pdl(lc.st, grid, dim3(128), (size_t)prefix_smem_bytes<HD, 4>(), sp.S, attn_prefix_mma<HD, 4>,
-                            tmK, tmV, a));
     }
     lc.after(SF_K_ATTN_PREFIX);
   }
@@ -1548,8 +1135,8 @@ cudaError_t attention_simt(Launch& lc, const AttnArgs& a) {
 cudaError_t launch_attention(Launch& lc, int act_bf16, const AttnArgs& a) {
   if (a.hd > kMaxHd || a.hd % 32 != 0 || a.L > kKB) return cudaErrorInvalidValue;
   if (!act_bf16) return attention_simt<float>(lc, a);
-  if (a.hd == 128) return attention_mma<128>(lc, a);
-  if (a.hd == 64) return attention_mma<64>(lc, a);
+  if (a.hd == 128) return attention_tc<128>(lc, a);
+  if (a.hd == 64) return attention_tc<64>(lc, a);
   return cudaErrorInvalidValue;
 }
 

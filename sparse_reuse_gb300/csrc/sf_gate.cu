@@ -265,6 +265,246 @@ __device__ __forceinline__ unsigned gate_word(const GateArgs& a, int j, unsigned
   return (unsigned)(v >> 32) == tag ? ((unsigned)v & 1u) : gate_word_wait(a, j, tag, v);
 }
 
+// Gate, compaction, source resolution and attention RMSNorm of one layer in
+// one launch, one CTA per row.  Each CTA takes an arrival ticket and handles
+// row = ticket, so rows are handed out in ascending order and every lower row
+// belongs to a CTA that is already running:
+//   1. the row's layer input H (previous layer's residual applied, written
+//      out) and its gate decision against the parent row: VEC float4 columns
+//      a thread (256 threads cover rows of up to VEC * 1024 features), every
+//      load of the row and of its parent row issued before the first is used;
+//   2. it publishes the decision in its gate word (release);
+//   3. warp 0 finds the row's source, the nearest row up its chain (itself,
+//      its parent's row, ...) that recomputes, from those rows' words, and the
+//      CTA counts the recompute rows below the row and below the source from
+//      the words of all lower rows (256 threads read them at once): the counts
+//      are the slots of the row and of its source in the stable ascending
+//      recompute list;
+//   4. a recompute row writes its list entry and its normalised row at its
+//      slot, from the registers that still hold H.
+// A CTA waits only for lower rows, whose CTAs never wait for higher ones, so
+// every wait ends whatever the number of resident CTAs; the waits are
+// bounded all the same.
+template <bool kLayer0, typename TIn, int VEC, typename TAct>
+__global__ void __launch_bounds__(kGateThreads, VEC <= 2 ? 5 : 3) gate_scan_kernel(const __grid_constant__ GateArgs a) {
+  __shared__ float red[3][32];
+  __shared__ int cnt[2][32];
+  __shared__ int s_row, s_srow, s_src, s_slot;
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    const unsigned t = atomicAdd(a.ticket, 1u);
+    if (t == (unsigned)a.T - 1u) *a.ticket = 0u;  // every ticket of this launch is taken
+    s_row = (int)t;
+  }
+  __syncthreads();
+  const int row = s_row;
+  const int L = a.L, Bp = a.tree.Bp;
+  const int n = row % L, rb = row / L, i = rb % Bp, r = rb / Bp;
+  const int prow = i > 0 ? (r * Bp + a.tree.parent[r * Bp + i]) * L + n : -1;
+  const int d4 = a.d >> 2;
+  const unsigned tag = scan_tag(a);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = kGateThreads / 32;
+
+  // 1. the layer input of the row and of its parent row
+  float4 xs[VEC], ys[VEC];
+  if constexpr (kLayer0) {
+    const TIn* xr = reinterpret_cast<const TIn*>(a.x_in) + (size_t)row * a.d;
+    const TIn* yr = reinterpret_cast<const TIn*>(a.x_in) + (size_t)(prow >= 0 ? prow : row) * a.d;
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * kGateThreads;
+      if (c < d4) {
+        xs[k] = load4<TIn>(xr + c * 4);
+        if (prow >= 0) ys[k] = load4<TIn>(yr + c * 4);
+      }
+    }
+  } else {
+    // the previous layer's last residual add: H = h + f[source slot]; the
+    // parent's input is recomputed from the same operands, so it is
+    // bit-identical to what the parent's CTA writes
+    const float4* hx = reinterpret_cast<const float4*>(a.h_prev + (size_t)row * a.d);
+    const float4* fx = reinterpret_cast<const float4*>(a.f_prev + (size_t)a.rcslot_prev[row] * a.d);
+    const float4* hy = reinterpret_cast<const float4*>(a.h_prev + (size_t)(prow >= 0 ? prow : row) * a.d);
+    const float4* fy =
+        reinterpret_cast<const float4*>(a.f_prev + (size_t)a.rcslot_prev[prow >= 0 ? prow : row] * a.d);
+    float4 fxs[VEC], fys[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const int c = threadIdx.x + k * kGateThreads;
+      if (c < d4) {
+        xs[k] = hx[c];
+        fxs[k] = fx[c];
+        if (prow >= 0) {
+          ys[k] = hy[c];
+          fys[k] = fy[c];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      xs[k] = make_float4(xs[k].x + fxs[k].x, xs[k].y + fxs[k].y, xs[k].z + fxs[k].z, xs[k].w + fxs[k].w);
+      if (prow >= 0)
+        ys[k] = make_float4(ys[k].x + fys[k].x, ys[k].y + fys[k].y, ys[k].z + fys[k].z, ys[k].w + fys[k].w);
+    }
+  }
+  float diff2 = 0.f, par2 = 0.f, ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    const int c = threadIdx.x + k * kGateThreads;
+    if (c < d4) {
+      const float4 x = xs[k];
+      *reinterpret_cast<float4*>(a.H_out + (size_t)row * a.d + c * 4) = x;
+      if (a.dbg) *reinterpret_cast<float4*>(a.dbg + (size_t)row * a.d + c * 4) = x;
+      ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+      if (prow >= 0) {
+        const float4 y = ys[k];
+        const float dx = x.x - y.x, dy = x.y - y.y, dz = x.z - y.z, dw = x.w - y.w;
+        diff2 += dx * dx + dy * dy + dz * dz + dw * dw;
+        par2 += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+      }
+    }
+  }
+  // the three sums in one exchange, added in the same order as block_sum
+  diff2 = warp_sum(diff2);
+  par2 = warp_sum(par2);
+  ss = warp_sum(ss);
+  if (lane == 0) {
+    red[0][warp] = diff2;
+    red[1][warp] = par2;
+    red[2][warp] = ss;
+  }
+  __syncthreads();
+  diff2 = warp_sum(lane < kWarps ? red[0][lane] : 0.f);
+  par2 = warp_sum(lane < kWarps ? red[1][lane] : 0.f);
+  ss = warp_sum(lane < kWarps ? red[2][lane] : 0.f);
+  // rho <= delta  <=>  ||diff||^2 <= delta^2 ||parent||^2 (covers a zero parent)
+  const int f = (prow >= 0 && a.delta > 0.f && diff2 <= a.delta * a.delta * par2) ? 1 : 0;
+
+  // 2. the decision
+  if (threadIdx.x == 0) {
+    a.fold[row] = (uint8_t)f;
+    if (a.fold_user) a.fold_user[row] = (uint8_t)f;
+    if (a.rho_user)
+      a.rho_user[row] = prow < 0 ? __int_as_float(0x7fc00000)
+                                 : (par2 > 0.f ? sqrtf(diff2 / par2) : (diff2 > 0.f ? __int_as_float(0x7f800000) : 0.f));
+    if (!(a.stall && row == 0))  // failure injection: row 0 never reports
+      st_release_u64(a.scan + row, ((unsigned long long)tag << 32) | (f ? 0u : 1u));
+  }
+
+  // 3. the source, then the recompute rows below the row and below the source
+  if (warp == 0) {
+    if (!f) {
+      if (lane == 0) {
+        s_srow = row;
+        s_src = i;
+      }
+    } else {
+      // lane k reads the word of the k-th row up the chain from the parent
+      // (32 at a time); the main branch always recomputes
+      int start = a.tree.parent[r * Bp + i];
+      for (;;) {
+        int b = start;
+        for (int k = 0; k < lane && b >= 0; ++k) b = a.tree.parent[r * Bp + b];
+        const bool on = b >= 0;
+        const unsigned rc = on ? gate_word(a, (r * Bp + b) * L + n, tag) : 0u;
+        const unsigned hits = __ballot_sync(0xffffffffu, on && rc);
+        if (hits) {
+          const int src = __shfl_sync(0xffffffffu, b, __ffs(hits) - 1);
+          if (lane == 0) {
+            s_srow = (r * Bp + src) * L + n;
+            s_src = src;
+          }
+          break;
+        }
+        const int last = __shfl_sync(0xffffffffu, b, 31);
+        start = last >= 0 ? a.tree.parent[r * Bp + last] : -1;
+        if (start < 0) {  // cannot happen for a validated tree
+          if (lane == 0) {
+            raise_error(a.err, kErrGate);
+            s_srow = r * Bp * L + n;
+            s_src = 0;
+          }
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int srow = s_srow;
+  int below = 0, below_src = 0;
+  for (int j0 = 0; j0 < row; j0 += 4 * kGateThreads) {
+    unsigned long long w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = j0 + threadIdx.x + k * kGateThreads;
+      w[k] = j < row ? ld_acquire_u64(a.scan + j) : 0ull;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = j0 + threadIdx.x + k * kGateThreads;
+      if (j < row) {
+        const unsigned rc = (unsigned)(w[k] >> 32) == tag ? ((unsigned)w[k] & 1u) : gate_word_wait(a, j, tag, w[k]);
+        below += rc;
+        below_src += j < srow ? rc : 0;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    below += __shfl_xor_sync(0xffffffffu, below, o);
+    below_src += __shfl_xor_sync(0xffffffffu, below_src, o);
+  }
+  if (lane == 0) {
+    cnt[0][warp] = below;
+    cnt[1][warp] = below_src;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tot = 0, tot_src = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      tot += cnt[0][w];
+      tot_src += cnt[1][w];
+    }
+    const int slot = f ? tot_src : tot;
+    if (!f) {
+      a.rc[slot] = row;
+      if (a.rc_user) a.rc_user[slot] = row;
+      if (i == 0 && n == 0) a.meta[1 + r] = slot;  // first recompute row of request r
+    }
+    a.rcslot[row] = slot;
+    if (a.src_user) a.src_user[row] = s_src;
+    if (row == a.T - 1) {
+      const int total = tot + (f ? 0 : 1);
+      a.meta[0] = total;
+      a.meta[1 + a.tree.R] = total;
+      if (a.rc_count_user) *a.rc_count_user = total;
+    }
+    s_slot = slot;
+  }
+  if (f) return;
+  __syncthreads();
+
+  // 4. the normalised row of a recompute row
+  const float rstd = rsqrtf(ss / (float)a.d + a.eps);
+  TAct* out = reinterpret_cast<TAct*>(a.xn) + (size_t)s_slot * a.d;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    const int c = threadIdx.x + k * kGateThreads;
+    if (c < d4) {
+      const float4 v = xs[k];
+      const float4 w = *reinterpret_cast<const float4*>(a.gain + c * 4);
+      store4<TAct>(out + c * 4, make_float4(v.x * rstd * w.x, v.y * rstd * w.y, v.z * rstd * w.z, v.w * rstd * w.w));
+    }
+  }
+}
+
+// Wide rows (more than 4 float4 a thread): the gate in two launches, which
+// overlap better than one kernel whose register-heavy CTAs run in several
+// waves.
+//
 // Gate, part 1: the layer input and the gate decision of every row.  CTA =
 // one row, VEC float4 columns per thread (256 threads cover rows of up to
 // VEC * 1024 features), every load of the row and of its parent row issued
@@ -646,8 +886,22 @@ cudaError_t launch_gate(Launch& lc, const GateArgs& a, int in_bf16) {
 namespace {
 
 template <int VEC>
+cudaError_t launch_gate_scan(Launch& lc, const GateArgs& a, int bf16) {
+  // layer 0 reads the block input, which has the context dtype like the
+  // normalised rows
+  auto k = a.x_in == nullptr
+               ? (bf16 ? gate_scan_kernel<false, float, VEC, __nv_bfloat16> : gate_scan_kernel<false, float, VEC, float>)
+               : (bf16 ? gate_scan_kernel<true, __nv_bfloat16, VEC, __nv_bfloat16>
+                       : gate_scan_kernel<true, float, VEC, float>);
+  return launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), 0, 1, k, a);
+}
+
+}  // namespace
+
+namespace {
+
+template <int VEC>
 cudaError_t launch_gate_rows(Launch& lc, const GateArgs& a, int bf16) {
-  // layer 0 reads the block input, which has the context dtype
   auto k = a.x_in == nullptr ? gate_rows_kernel<false, float, VEC>
                              : (bf16 ? gate_rows_kernel<true, __nv_bfloat16, VEC> : gate_rows_kernel<true, float, VEC>);
   return launch_pdl(lc.st, dim3(a.T), dim3(kGateThreads), 0, 1, k, a);
@@ -657,15 +911,21 @@ cudaError_t launch_gate_rows(Launch& lc, const GateArgs& a, int bf16) {
 
 cudaError_t launch_gate_norm(Launch& lc, const GateArgs& a, int bf16) {
   const int per = (a.d / 4 + kGateThreads - 1) / kGateThreads;  // float4 columns a thread
-  if (a.d % 4 != 0 || per > 16 || !a.xn || !a.gain || !a.scan || !a.epoch || !a.row_ss || a.T < 1)
+  if (a.d % 4 != 0 || per > 16 || !a.xn || !a.gain || !a.scan || !a.epoch || !a.ticket || !a.row_ss || a.T < 1)
     return lc.err = cudaErrorInvalidValue;
-  // two launches, each bracketed (counted and, when selected, timed) on its own
+  if (per <= 4) {
+    lc.before(SF_K_GATE);
+    if (per <= 2)
+      lc.check(launch_gate_scan<2>(lc, a, bf16));
+    else
+      lc.check(launch_gate_scan<4>(lc, a, bf16));
+    lc.after(SF_K_GATE);
+    return lc.err;
+  }
+  // wide rows: two launches, each bracketed (counted and, when selected,
+  // timed) on its own
   lc.before(SF_K_GATE);
-  if (per <= 2)
-    lc.check(launch_gate_rows<2>(lc, a, bf16));
-  else if (per <= 4)
-    lc.check(launch_gate_rows<4>(lc, a, bf16));
-  else if (per <= 6)
+  if (per <= 6)
     lc.check(launch_gate_rows<6>(lc, a, bf16));
   else if (per <= 8)
     lc.check(launch_gate_rows<8>(lc, a, bf16));

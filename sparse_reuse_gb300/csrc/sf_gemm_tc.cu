@@ -451,11 +451,28 @@ cudaError_t launch_tc(const TcGemm& g, const typename Epi::Params& ep, cudaStrea
   const int pipe = base - ((staged + 1023) & ~1023);
   if (tc::stages_for(pipe, 0) < 2) return cudaErrorInvalidValue;
   // a dense row count is split into equal row tiles (multiples of 16, the
-  // MMA's N step), so no tile carries a short remainder
+  // MMA's N step), so no tile carries a short remainder; with more tiles than
+  // SMs the tile count is the one with the shortest busiest SM: tiles per SM
+  // (rounded up) times rows per tile
   int tile = tc::BN, n_tiles = (g.max_rows + tc::BN - 1) / tc::BN;
   if (!g.count && g.dense_count > 0) {
     n_tiles = (g.dense_count + tc::BN - 1) / tc::BN;
     tile = ((g.dense_count + n_tiles - 1) / n_tiles + 15) & ~15;
+    if (base == tc::PIPE_BYTES_PAIR) {
+      const int m_tiles = g.M / tc::BM, sms = sm_count();
+      long best = -1;
+      for (int n = n_tiles; n <= 2 * n_tiles + 4; ++n) {
+        const int t = ((g.dense_count + n - 1) / n + 15) & ~15;
+        const int used = (g.dense_count + t - 1) / t;
+        if (t < 64 || m_tiles * used > 2 * sms) continue;  // all tiles resident, two per SM at most
+        const long cost = (long)((m_tiles * used + sms - 1) / sms) * t;
+        if (best < 0 || cost < best) {
+          best = cost;
+          n_tiles = used;
+          tile = t;
+        }
+      }
+    }
   }
   tc::Params p{g.M, g.K, g.count, g.dense_count, g.splits, g.err, pipe, g.count_early ? 1 : 0, tile};
   return launch_pdl(st, dim3(g.M / tc::BM, n_tiles, g.splits), dim3(tc::THREADS),

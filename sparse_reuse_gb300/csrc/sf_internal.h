@@ -78,7 +78,7 @@ struct sf_ctx {
   unsigned* ticket = nullptr;
   unsigned* epoch = nullptr;  // [0] pass counter
   unsigned long long* scan = nullptr;  // [T_max] the gate's per-row words
-  float* gate_ss = nullptr;            // [T_max] ||H||^2 per row
+  float* gate_ss = nullptr;            // [T_max] ||H||^2 per row (wide-row gate)
   unsigned* err_dev = nullptr;
   unsigned* err_host = nullptr;  // pinned mirror, refreshed at the end of every pass
   float2* rope = nullptr;   // [max_pos][hd/2] (cos, sin), computed in double on the host
@@ -177,7 +177,7 @@ struct GateArgs {
   const float* gain;      // [d] attention RMSNorm gain
   float eps;
   unsigned long long* scan;  // [T] per-row gate words (tag | recompute bit)
-  float* row_ss;             // [T] ||H||^2 of the row, for the attention RMSNorm
+  float* row_ss;             // [T] ||H||^2 of every row (wide-row gate: part 1 to part 2)
   float* rho_user;           // [T] or nullptr: rho of every row (NaN for the main branch)
   int stall;                 // failure injection: row 0 never reports, so the waits on it run out
   const unsigned* epoch;     // pass counter, advanced by the final residual kernel

@@ -84,3 +84,33 @@ def test_modes_agree_on_the_first_layer():
     b, _ = _run(cfg, wl, 0.1, sf.SF_ATTN_CORRECT)
     assert np.array_equal(a["fold"], b["fold"])
     np.testing.assert_allclose(b["out"], a["out"], rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(n_requests=3, n_q_heads=7, n_kv_heads=1, prefix_len=200, n_drafts=4),
+                                dict(prefix_len=2100, head_dim=64, n_q_heads=8, n_kv_heads=2, block_len=20,
+                                     n_drafts=5),
+                                dict(prefix_len=1000, n_drafts=2, block_len=64)])
+def test_bf16_split_kernels_teacher_forced(kw):
+    """SF_ATTN_DIRECT_SPLIT: the prefix-partial + block kernels that long
+    prefixes take, forced on the small shapes that otherwise run fused."""
+    import sparse_reuse_gb300 as sf
+    base = dict(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=128, d_ffn=320, dtype="bf16",
+                block_len=32, prefix_len=96, n_drafts=4)
+    base.update(kw)
+    cfg = synth.small_config(**base)
+    wl = synth.make_workload(cfg, seed=34, device="cuda")
+    for delta in (0.0, 0.1):
+        gpu, st = _run(cfg, wl, delta, sf.SF_ATTN_DIRECT_SPLIT)
+        assert st["family_launches"]["attn_block"] == cfg.n_layers
+        check_teacher_forced(cfg, wl, gpu, delta, range(cfg.n_layers))
+
+
+def test_fused_attention_runs_one_kernel_per_layer():
+    """Short prefixes in the default mode: no block kernel at all."""
+    import sparse_reuse_gb300 as sf
+    cfg = synth.small_config(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=128, d_ffn=320,
+                             dtype="bf16", block_len=32, prefix_len=512, n_drafts=4)
+    wl = synth.make_workload(cfg, seed=35, device="cuda")
+    gpu, st = _run(cfg, wl, 0.1, sf.SF_ATTN_DIRECT)
+    assert st["family_launches"]["attn_block"] == 0 and st["family_launches"]["attn_prefix"] == cfg.n_layers
+    check_teacher_forced(cfg, wl, gpu, 0.1, range(cfg.n_layers))

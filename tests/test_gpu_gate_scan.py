@@ -93,3 +93,24 @@ def test_rho_dump_matches_oracle_on_gpu_layer_inputs():
         for r in range(R):
             _, want = oracle.gate_request(H_in[r], wl.parents[r], 0.1)
             np.testing.assert_allclose(got[l, r, 1:], want[1:], rtol=1e-4, atol=1e-6)
+
+
+@pytest.mark.parametrize("delta", [0.0, 0.1])
+def test_bf16_wide_rows_2304_teacher_forced(delta):
+    """d = 5120 (more than 4 float4 a thread): the two-launch gate, at 2,304
+    rows (several waves of its register-heavy first kernel)."""
+    cfg = synth.small_config(n_layers=2, d_model=5120, n_q_heads=4, n_kv_heads=2, head_dim=128, d_ffn=256,
+                             dtype="bf16", block_len=32, prefix_len=16, n_requests=8, n_drafts=8)
+    assert cfg.rows == 2304
+    wl = synth.make_workload(cfg, seed=15, device="cuda")
+    gpu = _checked_run(cfg, wl, delta)
+    assert gpu["stats"]["family_launches"]["gate"] == 2 * cfg.n_layers
+    check_teacher_forced(cfg, wl, gpu, delta, range(cfg.n_layers))
+
+
+def test_fp32_wide_rows_free_running():
+    cfg = synth.CONFIGS["tiny"].with_(n_layers=2, d_model=5120, n_q_heads=4, n_kv_heads=2, head_dim=64, d_ffn=256,
+                                      n_drafts=4, tree="random", unmask_exact=None)
+    wl = synth.make_workload(cfg, seed=16, device="cuda")
+    gpu = _checked_run(cfg, wl, 0.1)
+    check_free_running(cfg, wl, gpu, 0.1)
