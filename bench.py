@@ -84,14 +84,20 @@ def pass_work(cfg, rc_counts):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
-# from the committed ncu capture of the current kernels (the 1.5B GEMM
-# summary under profiles/).  A kernel changed since its capture has no entry
-# (traffic is then reported as null).
+# from the committed ncu captures of the current kernels (the 1.5B GEMM and
+# the 14B layer summaries under profiles/).  A kernel changed since its
+# capture has no entry (traffic is then reported as null).
 NCU_TRAFFIC = {
     ("1.5b", "gemm_gateup"): 55.29e6,
     ("1.5b", "gemm_down"): 28.70e6,
     ("1.5b", "gemm_o"): 7.57e6,
     ("1.5b", "gemm_qkv"): 6.55e6,
+    ("14b", "gemm_gateup"): 288.85e6,
+    ("14b", "gemm_down"): 151.71e6,
+    ("14b", "gemm_o"): 91.63e6,
+    ("14b", "gemm_qkv"): 77.29e6,
+    ("14b", "attn_prefix"): 70.99e6,
+    ("14b", "attn_block"): 7.01e6,
 }
 
 
