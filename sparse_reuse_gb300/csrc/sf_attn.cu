@@ -82,28 +82,41 @@ using bf16 = __nv_bfloat16;
 //
 // Prefix partials on the 5th-generation tensor cores: CTA = (128 query vectors
 // of one request and KV head = the 128 TMEM lanes, one split of the prefix).
-// Per block of 64 keys:
-//   S = Q K^T       tcgen05.mma, Q and K K-major in shared memory, S in TMEM
-//                   (three buffers: the scores two blocks ahead are computed
-//                   while this block's softmax runs);
-//   P = exp2(S - m) by the softmax warps, one query row per thread, written as
-//                   bf16 to shared memory (K-major, 128-byte swizzle);
-//   O += P V        tcgen05.mma, V MN-major as the TMA box leaves it, O in TMEM.
+// The queries are written once into TMEM as bf16 pairs; per block of 64 keys:
+//   S = Q K^T       tcgen05.mma with Q from TMEM and K K-major in shared
+//                   memory, S in TMEM (three buffers: the scores two blocks
+//                   ahead are computed while this block's softmax runs);
+//   P = exp2(S - m) by the softmax warps, one query row per thread, written
+//                   back to TMEM as bf16 pairs (two buffers);
+//   O += P V        tcgen05.mma with P from TMEM and V MN-major as the TMA
+//                   box leaves it, O in TMEM.
+// Shared memory then carries only the K and V rings, so each block costs
+// the TMA writes and one tensor-core read of its keys and values.
 // The running max m of a row only moves when a block's max exceeds it by more
 // than 2^8, and O is then rescaled in TMEM; the partial state (m, l, O) stays
 // exact because m is whatever reference the exponentials used.
-// Warp 0 streams K and V through two kTcStages-deep rings of TMA loads (lane 0
-// the keys, freed once their scores are computed; lane 1 the values, freed
-// once P V is done), warp 1 owns TMEM and issues the MMAs, warps 2-9 load Q and
-// run the softmax and the epilogue: the two warps on the same 32 TMEM lanes
-// take half of each row's 64 scores and half of its output columns, and
-// exchange only the row's block maximum.
-// The split CTAs of a tile form a cluster and merge as the CUDA-core path does.
+// Warp 0 streams the keys through a kTcStages-deep ring of TMA loads (a stage
+// is freed once its scores are computed), warp 10 the values (freed once P V
+// is done), warp 1 owns TMEM and issues the score MMAs, warp 11 the P V MMAs,
+// warps 2-9 load Q and run the softmax and the epilogue: the two warps on the
+// same 32 TMEM lanes take half of each row's 64 scores and half of its output
+// columns, and exchange only the row's block maximum.  Every role that waits
+// on barriers has a warp of its own: a lane spinning on one barrier holds back
+// a diverged lane of its warp, and one thread issuing both MMA groups leaves
+// the tensor core idle during its barrier waits (its queue is short).
+// With several splits, the splits of a query tile form a cluster: every split
+// stores its partial state in a slot of its own (part_o / part_ml slots
+// 1..S), the cluster meets at a barrier, and split s merges rows
+// [s per, (s + 1) per) of the tile from the S slots.
 constexpr int kTcQ = 128;
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per row group)
+// warp 0 K loads, warp 1 S = Q K^T, warps 2-9 softmax (two per row group), warp 10 V loads, warp 11 O += P V
+constexpr int kTcThreads = 384;
+constexpr int kTcVWarp = 10;
+constexpr int kTcPVWarp = 11;
 constexpr int kTcMinKeysPerSplit = 512;
 constexpr int kTcMaxSplits = 4;
+static_assert(1 + kTcMaxSplits <= kMaxSplits, "split slots of the partial buffers");
 // Prefixes of at least this many keys take the tcgen05 kernel.
 constexpr int kTcMinPrefix = 1;
 constexpr float kTcRescaleLog2 = 8.f;
@@ -142,18 +155,15 @@ inline Splits fused_splits(int P, int ctas, int target_ctas) {
   return tc_split_len(P, S);
 }
 
-template <int HD, int STAGES = kTcStages>
+template <int HD>
 struct TcLayout {
-  static constexpr int ST = STAGES;                     // K (and V) ring stages
+  static constexpr int ST = kTcStages;                  // K (and V) ring stages
   static constexpr int QH = HD / 64;                    // 64-dim halves
-  static constexpr int HALF = kTcQ * 128;               // one 64-dim half of Q: 128 rows x 128 B
   static constexpr int KV_TILE = kKB * 128;             // one 64-dim half of a K or V block
   static constexpr int STAGE = QH * KV_TILE;            // K (or V) of one block
-  static constexpr int P_TILE = kTcQ * 128;             // P: 128 rows x 64 keys (bf16)
-  static constexpr int OFF_K = QH * HALF;
-  static constexpr int OFF_V = OFF_K + ST * STAGE;
-  static constexpr int OFF_P = OFF_V + ST * STAGE;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = ST * STAGE;
+  static constexpr int OFF_BAR = 2 * ST * STAGE;
   static constexpr int BYTES = OFF_BAR + 256 + 1024;   // + alignment of the dynamic window
   // fused variant: the branch's own block keys and values (one 64-key block,
   // gathered), after the barriers; 128-byte-swizzled tiles start on a
@@ -161,14 +171,16 @@ struct TcLayout {
   static constexpr int OFF_BK = (OFF_BAR + 256 + 1023) / 1024 * 1024;
   static constexpr int OFF_BV = OFF_BK + STAGE;
   static constexpr int BYTES_FUSED = OFF_BV + STAGE + 1024;
-  static constexpr int XLD = HD + 4;                    // merge exchange row: o[HD], m, l (16-byte rows)
   static constexpr int SBUF = 3;                        // score buffers: columns [64 s, 64 s + 64)
+  static constexpr int Q_COL = SBUF * kKB;              // Q: HD / 2 columns of bf16 pairs
   static constexpr int O_COL = 256;                     // O: columns [256, 256 + HD)
+  static constexpr int P_COL = O_COL + HD;              // P: two buffers of kKB / 2 columns of bf16 pairs
   static constexpr int TMEM_COLS = 512;
-  static_assert((kTcQ + kMaxSplits - 1) * XLD * 4 <= OFF_P, "merge exchange area");
-  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && OFF_BK % 1024 == 0 &&
-                    OFF_BV % 1024 == 0,
+  static_assert(Q_COL + HD / 2 <= O_COL && P_COL + kKB <= TMEM_COLS, "TMEM columns");
+  static_assert((4 * ST + 2 * SBUF + 6) * 8 + 8 <= 256, "barrier area");
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_BK % 1024 == 0 && OFF_BV % 1024 == 0,
                 "swizzled tiles on 1024-byte boundaries");
+  static_assert(BYTES_FUSED <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ void tmem_ld32_raw(uint32_t taddr, float (&v)[32]) { tc::tmem_ld32(taddr, v); }
@@ -192,49 +204,45 @@ template <int HD, bool kFused>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_constant__ CUtensorMap tmK,
                                                                 const __grid_constant__ CUtensorMap tmV,
                                                                 const AttnArgs a) {
-  // the fused variant keeps three K/V stages, which leaves room for the
-  // branch's block keys and values
-  using Lay = TcLayout<HD, kFused ? 3 : kTcStages>;
+  using Lay = TcLayout<HD>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  unsigned char* sQ = base;
   unsigned char* sK = base + Lay::OFF_K;
   unsigned char* sV = base + Lay::OFF_V;
-  unsigned char* sP = base + Lay::OFF_P;
   uint64_t* bar = reinterpret_cast<uint64_t*>(base + Lay::OFF_BAR);
   uint64_t* kfull = bar;                   // [Lay::ST] K landed
-  uint64_t* vfull = bar + Lay::ST;       // [Lay::ST] V landed
-  uint64_t* kempty = bar + 2 * Lay::ST;  // [Lay::ST] K consumed by S = Q K^T
-  uint64_t* vempty = bar + 3 * Lay::ST;  // [Lay::ST] V consumed by O += P V
-  uint64_t* sfull = bar + 4 * Lay::ST;   // [SBUF] scores in TMEM
+  uint64_t* vfull = bar + Lay::ST;         // [Lay::ST] V landed
+  uint64_t* kempty = bar + 2 * Lay::ST;    // [Lay::ST] K consumed by S = Q K^T
+  uint64_t* vempty = bar + 3 * Lay::ST;    // [Lay::ST] V consumed by O += P V
+  uint64_t* sfull = bar + 4 * Lay::ST;     // [SBUF] scores in TMEM
   uint64_t* sempty = sfull + Lay::SBUF;    // [SBUF] scores read
   uint64_t* pfull = sempty + Lay::SBUF;    // [2] P written
   uint64_t* pvdone = pfull + 2;            // [2] P V of that buffer done
   uint64_t* qready = pvdone + 2;
   uint64_t* ofull = qready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
-  float* xbuf = reinterpret_cast<float*>(base);  // merge exchange, over Q and the ring once they are dead
   __shared__ float xmax[2][2][kTcQ];             // [block parity][half][row]: partial block maxima
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // grid: x = (request, KV head) -- fused: (branch, KV head) --, y = query
-  // tile, z = split; the first query tiles of every x are dispatched first,
-  // and the tiles that only a larger recompute set would fill come last
-  const int xr = blockIdx.x / a.nkv, kvh = blockIdx.x % a.nkv;
+  // grid: x = split, y = (request, KV head) -- fused: (branch, KV head) --,
+  // z = query tile; the splits of a tile and the first query tiles of every y
+  // are dispatched first, the tiles that only a larger recompute set would
+  // fill come last
+  const int xr = blockIdx.y / a.nkv, kvh = blockIdx.y % a.nkv;
   const int r = kFused ? xr / a.Bp : xr;
-  const Splits sp = tc_split_len(a.P, (int)gridDim.z);
+  const Splits sp = tc_split_len(a.P, (int)gridDim.x);
   const int G = a.nq / a.nkv;
   // recompute offsets from the gate kernel (complete once this grid runs), past L1
   const int off_r = kFused ? 0 : __ldcg(a.meta + 1 + r);
   const int nqv = kFused ? a.L * G : (__ldcg(a.meta + 2 + r) - off_r) * G;
-  const int q0 = blockIdx.y * kTcQ;
+  const int q0 = blockIdx.z * kTcQ;
   // An empty tile leaves without the dependency wait: it reads nothing of the
   // previous kernel, and the live tiles (the main branch always recomputes,
   // so there is one per request and KV head) still hold the next kernel back
-  // until they have waited.  Uniform over the cluster.
+  // until they have waited.  Every split of a tile agrees.
   if (q0 >= nqv) return;
-  const int s = sp.S > 1 ? (int)tc::cluster_ctarank() : 0;
+  const int s = (int)blockIdx.x;
   const int k_lo = s * sp.len, k_hi = min(a.P, k_lo + sp.len);
   const int nblk_p = (k_hi - k_lo + kKB - 1) / kKB;  // prefix blocks of this split
   // fused: the last split takes the branch's block keys as one more block
@@ -266,8 +274,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // warp 0: lane 0 loads key block b into K stage b % Lay::ST, lane 1 the
-  // value block into the V ring
+  // lane 0 of warp 0 loads key block b into K stage b % Lay::ST, lane 0 of
+  // warp 10 the value block into the V ring
   auto issue = [&](int b, bool keys) {
     const int st = b % Lay::ST;
     unsigned char* dst = (keys ? sK : sV) + st * Lay::STAGE;
@@ -278,15 +286,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
     for (int h = 0; h < Lay::QH; ++h) tc::tma_load_3d(dst + h * Lay::KV_TILE, keys ? &tmK : &tmV, h * 64, kvh, z, full);
   };
   // the prefix keys and values are inputs of the pass
-  if (warp == 0 && lane < 2)
-    for (int b = 0; b < min(Lay::ST, nblk_p); ++b) issue(b, lane == 0);
+  const bool producer = (warp == 0 || warp == kTcVWarp);
+  if (producer && lane == 0)
+    for (int b = 0; b < min(Lay::ST, nblk_p); ++b) issue(b, warp == 0);
   pdl_wait();
   pdl_trigger();
 
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
-  if (warp == 0) {
-    if (lane < 2) {
-      const bool keys = lane == 0;
+  if (producer) {
+    if (lane == 0) {
+      const bool keys = warp == 0;
       for (int b = Lay::ST; b < nblk_p; ++b) {
         // the stage is free once the MMA that read block b - Lay::ST has completed
         tc::mbar_wait(keys ? &kempty[b % Lay::ST] : &vempty[b % Lay::ST], ((b / Lay::ST) - 1) & 1, a.err);
@@ -294,54 +303,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kTcPVWarp) {
     if (lane == 0) {
-      const uint32_t idesc_s = tc::idesc_bf16_f32(kTcQ, kKB);
-      const uint32_t idesc_pv = tc::idesc_bf16_f32(kTcQ, HD) | (1u << 16);  // V is MN-major
+      // A descriptor's address field is the shared-memory address in 16-byte
+      // units, so the descriptor of any tile of a ring is its first tile's
+      // plus the offset / 16: built once here
       tc::mbar_wait(qready, 0, a.err);
-      auto issue_s = [&](int b) {  // S(b) = Q K(b)^T into score buffer b % SBUF
-        const int st = b % Lay::ST, sb = b % Lay::SBUF;
-        const bool blk = b >= nblk_p;  // fused: the branch's block keys, ready with Q
-        if (!blk) tc::mbar_wait(&kfull[st], (b / Lay::ST) & 1, a.err);
-        if (b >= Lay::SBUF) tc::mbar_wait(&sempty[sb], ((b / Lay::SBUF) - 1) & 1, a.err);
-        tc::fence_after_sync();
-        const unsigned char* sk = blk ? base + Lay::OFF_BK : sK + st * Lay::STAGE;
+      tc::fence_after_sync();
+      if (warp == 1) {
+        const uint32_t idesc_s = tc::idesc_bf16_f32(kTcQ, kKB);
+        const uint64_t dk0 = tc::sw128_kmajor_desc(smem_addr(sK));
+        const uint64_t dbk = tc::sw128_kmajor_desc(smem_addr(base + Lay::OFF_BK));
+        // S(b) = Q K(b)^T into score buffer b % SBUF, up to SBUF blocks ahead of the softmax
+        for (int b = 0; b < nblk; ++b) {
+          const int st = b % Lay::ST, sb = b % Lay::SBUF;
+          const bool blk = b >= nblk_p;  // fused: the branch's block keys, ready with Q
+          if (!blk) tc::mbar_wait(&kfull[st], (b / Lay::ST) & 1, a.err);
+          if (b >= Lay::SBUF) tc::mbar_wait(&sempty[sb], ((b / Lay::SBUF) - 1) & 1, a.err);
+          tc::fence_after_sync();
+          const uint64_t dk = blk ? dbk : dk0 + (uint64_t)((st * Lay::STAGE) >> 4);
+          const uint32_t ds = tmem + sb * kKB;
+          // 16 query dimensions a step = 8 TMEM columns of bf16 pairs
+          tc::mma_bf16_ts(ds, tmem + Lay::Q_COL, dk, idesc_s, 0u);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t dq = tc::sw128_kmajor_desc(smem_addr(sQ + (kk >> 2) * Lay::HALF + (kk & 3) * 32));
-          const uint64_t dk = tc::sw128_kmajor_desc(smem_addr(sk + (kk >> 2) * Lay::KV_TILE + (kk & 3) * 32));
-          tc::mma_bf16(tmem + sb * kKB, dq, dk, idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 1; kk < HD / 16; ++kk)
+            tc::mma_bf16_ts(ds, tmem + Lay::Q_COL + kk * 8,
+                            dk + (uint64_t)(((kk >> 2) * Lay::KV_TILE + (kk & 3) * 32) >> 4), idesc_s, 1u);
+          tc::mma_commit(&sfull[sb]);
+          if (!blk) tc::mma_commit(&kempty[st]);
         }
-        tc::mma_commit(&sfull[sb]);
-        if (!blk) tc::mma_commit(&kempty[st]);
-      };
-      for (int b = 0; b < min(Lay::SBUF - 1, nblk); ++b) issue_s(b);
-      for (int j = 0; j < nblk; ++j) {
-        // the scores SBUF - 1 blocks ahead, as soon as their buffer is read
-        if (j + Lay::SBUF - 1 < nblk) issue_s(j + Lay::SBUF - 1);
-        // O += P(j) V(j)
-        const int st = j % Lay::ST, pb = j & 1;
-        const bool blk = j >= nblk_p;
-        tc::mbar_wait(&pfull[pb], (j >> 1) & 1, a.err);
-        if (!blk) tc::mbar_wait(&vfull[st], (j / Lay::ST) & 1, a.err);
-        tc::fence_after_sync();
-        const unsigned char* sv = blk ? base + Lay::OFF_BV : sV + st * Lay::STAGE;
+      } else {
+        const uint32_t idesc_pv = tc::idesc_bf16_f32(kTcQ, HD) | (1u << 16);  // V is MN-major
+        const uint64_t dv0 = tc::sw128_mnmajor_desc(smem_addr(sV), Lay::KV_TILE);
+        const uint64_t dbv = tc::sw128_mnmajor_desc(smem_addr(base + Lay::OFF_BV), Lay::KV_TILE);
+        for (int j = 0; j < nblk; ++j) {
+          // O += P(j) V(j)
+          const int st = j % Lay::ST, pb = j & 1;
+          const bool blk = j >= nblk_p;
+          tc::mbar_wait(&pfull[pb], (j >> 1) & 1, a.err);
+          if (!blk) tc::mbar_wait(&vfull[st], (j / Lay::ST) & 1, a.err);
+          tc::fence_after_sync();
+          const uint64_t dv = blk ? dbv : dv0 + (uint64_t)((st * Lay::STAGE) >> 4);
+          const uint32_t dp = tmem + Lay::P_COL + pb * (kKB / 2);
+          tc::mma_bf16_ts(tmem + Lay::O_COL, dp, dv, idesc_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kKB / 16; ++kk) {
-          const uint64_t dp = tc::sw128_kmajor_desc(smem_addr(sP + pb * Lay::P_TILE + kk * 32));
-          const uint64_t dv = tc::sw128_mnmajor_desc(smem_addr(sv + kk * 2048), Lay::KV_TILE);
-          tc::mma_bf16(tmem + Lay::O_COL, dp, dv, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 1; kk < kKB / 16; ++kk)  // 16 keys a step: 2048 bytes of V, 8 columns of P
+            tc::mma_bf16_ts(tmem + Lay::O_COL, dp + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc_pv, 1u);
+          tc::mma_commit(&pvdone[pb]);
+          if (!blk) tc::mma_commit(&vempty[st]);
         }
-        tc::mma_commit(&pvdone[pb]);
-        if (!blk) tc::mma_commit(&vempty[st]);
+        tc::mma_commit(ofull);
       }
-      tc::mma_commit(ofull);
     }
     __syncwarp();
   } else {
     // softmax warps: TMEM lanes 32 * (warp % 4) .. + 31, one query row per
     // thread pair; `half` selects 32 of the row's 64 scores and HD / 2 of its
-    // output columns
+    // query and output columns
     const int grp = warp & 3, half = (warp - 2) >> 2;
     const int row = 32 * grp + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * grp) << 16);
@@ -351,27 +369,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
       // fused: row (b, v / G) of the branch, whose query is its source's
       const int g = kFused ? __ldcg(a.rcslot + xr * a.L + (ok ? v / G : 0)) : off_r + (ok ? v / G : 0);
       const int h = kvh * G + (ok ? v % G : 0);
-      const bf16* src = qkv + (size_t)g * a.ld_qkv + h * HD;
-#pragma unroll
-      for (int c = half * (HD / 16); c < (half + 1) * (HD / 16); ++c)
-        cp_async16(sQ + (c >> 3) * Lay::HALF + row * 128 + (((c & 7) ^ (row & 7)) << 4), src + c * 8, ok);
-      if (kFused && with_block) {
-        // the branch's block keys and values: key m of the branch's table is
-        // the K/V row of its source slot (zero past L); 256 threads, 64 keys
-        const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
-        const int t = tid - 64;
-        for (int idx = t; idx < kKB * (HD / 8); idx += 256) {
-          const int m = idx / (HD / 8), c = idx % (HD / 8);
-          const int gm = m < a.L ? __ldcg(a.rcslot + xr * a.L + m) : 0;
-          const bf16* kr = qkv + (size_t)gm * a.ld_qkv;
-          const int off = (c >> 3) * Lay::KV_TILE + m * 128 + (((c & 7) ^ (m & 7)) << 4);
-          cp_async16(base + Lay::OFF_BK + off, kr + koff + c * 8, m < a.L);
-          cp_async16(base + Lay::OFF_BV + off, kr + voff + c * 8, m < a.L);
+      const uint4* src = reinterpret_cast<const uint4*>(qkv + (size_t)g * a.ld_qkv + h * HD + half * (HD / 2));
+      if constexpr (kFused) {
+        if (with_block) {
+          // the branch's block keys and values: key m of the branch's table is
+          // the K/V row of its source slot (zero past L); 256 threads, 64 keys
+          const int koff = (a.nq + kvh) * HD, voff = (a.nq + a.nkv + kvh) * HD;
+          const int t = tid - 64;
+          for (int idx = t; idx < kKB * (HD / 8); idx += 256) {
+            const int m = idx / (HD / 8), c = idx % (HD / 8);
+            const int gm = m < a.L ? __ldcg(a.rcslot + xr * a.L + m) : 0;
+            const bf16* kr = qkv + (size_t)gm * a.ld_qkv;
+            const int off = (c >> 3) * Lay::KV_TILE + m * 128 + (((c & 7) ^ (m & 7)) << 4);
+            cp_async16(base + Lay::OFF_BK + off, kr + koff + c * 8, m < a.L);
+            cp_async16(base + Lay::OFF_BV + off, kr + voff + c * 8, m < a.L);
+          }
         }
+        cp_async_commit();
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      tc::fence_proxy_async_smem();
+      // this thread's HD / 2 query dimensions as HD / 4 columns of bf16 pairs
+      uint32_t qr[HD / 4];
+#pragma unroll
+      for (int c = 0; c < HD / 16; ++c) {
+        const uint4 u = ok ? __ldcg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        qr[4 * c] = u.x;
+        qr[4 * c + 1] = u.y;
+        qr[4 * c + 2] = u.z;
+        qr[4 * c + 3] = u.w;
+      }
+      tc::tmem_st_u32<HD / 4>(tl + Lay::Q_COL + half * (HD / 4), qr);
+      tc::tmem_wait_st();
+      if constexpr (kFused) {
+        cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+      }
+      tc::fence_before_sync();
       tc::mbar_arrive(qready);
     }
     const float scale = a.scale_log2;
@@ -400,9 +432,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
             if (kb0 + k >= k_hi) sc[k] = -INFINITY;
         }
       }
-      float mx = sc[0];
+      // tree reduction: five dependent steps instead of 31
+      float mt[16];
 #pragma unroll
-      for (int k = 1; k < 32; ++k) mx = fmaxf(mx, sc[k]);
+      for (int k = 0; k < 16; ++k) mt[k] = fmaxf(sc[k], sc[k + 16]);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) mt[k] = fmaxf(mt[k], mt[k + w]);
+      const float mx = mt[0];
       // the row's block maximum: exchange with the partner warp (double-buffered by block parity)
       xmax[pbuf][half][row] = mx;
       tc::named_bar_sync(1 + grp, 64);
@@ -431,23 +469,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
         }
       }
       const float mneg = -m_ref * scale;
-      float ls = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[16];
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
         const float p0 = ex2_approx(fmaf(sc[k], scale, mneg)), p1 = ex2_approx(fmaf(sc[k + 1], scale, mneg));
-        ls += p0 + p1;
+        ls[(k >> 1) & 3] += p0 + p1;
         pk[k / 2] = pack_bf16(p0, p1);
       }
-      l += ls;
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // P buffer b % 2 is free once P V of block b - 2 is done
-      if (b >= 2) tc::mbar_wait(&pvdone[pbuf], ((b - 2) >> 1) & 1, a.err);
-      unsigned char* prow = sP + pbuf * Lay::P_TILE + row * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(prow + (((4 * half + c) ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      tc::fence_proxy_async_smem();
+      if (b >= 2) {
+        tc::mbar_wait(&pvdone[pbuf], ((b - 2) >> 1) & 1, a.err);
+        tc::fence_after_sync();
+      }
+      // keys 32 half .. + 31 of the block: columns 16 half .. + 15 of the buffer
+      tc::tmem_st_u32<16>(tl + Lay::P_COL + pbuf * (kKB / 2) + 16 * half, pk);
+      tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&pfull[pbuf]);
     }
@@ -459,104 +497,142 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
     const float mrow = m_ref * scale;
     tc::mbar_wait(ofull, 0, a.err);
     tc::fence_after_sync();
-    constexpr int HO = HD / 2;
-    float o[HO];
+    // Epilogue.  The rows go through shared memory (the K and V rings, idle
+    // once every MMA has completed) so that a warp stores and loads whole
+    // rows: one 16-byte piece a lane, 32 lanes on consecutive addresses.
+    constexpr int HO = HD / 2, XLD = HD + 4;  // padded rows: the staging stores hit distinct banks
+    float* xs = reinterpret_cast<float*>(base + Lay::OFF_K);
+    float* xml = xs + kTcQ * XLD;  // per row: m (log2 units), l
+    static_assert(kTcQ * (XLD + 2) * 4 <= 2 * Lay::ST * Lay::STAGE, "staging area within the rings");
 #pragma unroll
-    for (int c0 = 0; c0 < HO; c0 += 32)
-      tmem_ld32_raw(tl + Lay::O_COL + half * HO + c0, *reinterpret_cast<float(*)[32]>(o + c0));
-    if (sp.S == 1) {  // a single split: the partial is already the merged state
-      if (v < nqv) {
-        if constexpr (kFused) {
-          const float inv = 1.f / lrow;
-          bf16* dst = reinterpret_cast<bf16*>(a.attn) + (size_t)(xr * a.L + v / G) * a.ld_attn +
-                      (kvh * G + v % G) * HD + half * HO;
+    for (int c0 = 0; c0 < HO; c0 += 32) {
+      float o[32];
+      tmem_ld32_raw(tl + Lay::O_COL + half * HO + c0, o);
+      float* dst = xs + row * XLD + half * HO + c0;
 #pragma unroll
-          for (int c = 0; c < HO; c += 8)
-            *reinterpret_cast<uint4*>(dst + c) =
-                make_uint4(pack_bf16(o[c] * inv, o[c + 1] * inv), pack_bf16(o[c + 2] * inv, o[c + 3] * inv),
-                           pack_bf16(o[c + 4] * inv, o[c + 5] * inv), pack_bf16(o[c + 6] * inv, o[c + 7] * inv));
-        } else {
-          const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
-          float* po = a.part_o + qi * HD + half * HO;
+      for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+    }
+    if (half == 0) *reinterpret_cast<float2*>(xml + 2 * row) = make_float2(m_ref * scale, lrow);
+    tc::named_bar_sync(5, 256);
+    // rows of the tile by warp: row rr = sw, sw + 8, ...; lane c4 < HD / 4 holds columns 4 c4 .. + 3
+    const int sw = warp - 2;
+    const int c4 = lane;
+    const bool col_ok = c4 < HD / 4;
+    const int rows = min(kTcQ, nqv - q0);
+    auto vec_index = [&](int rr) {  // query vector (row of the layer) * nq + query head
+      const int vv = q0 + rr;
+      return (size_t)((kFused ? xr * a.L : off_r) + vv / G) * a.nq + kvh * G + vv % G;
+    };
+    auto write_final = [&](int rr, float4 acc, float M, float lsum) {
+      const size_t qv = vec_index(rr);
+      if constexpr (kFused) {
+        const float inv = 1.f / lsum;
+        const int vv = q0 + rr;
+        bf16* dst = reinterpret_cast<bf16*>(a.attn) + (size_t)(xr * a.L + vv / G) * a.ld_attn + (kvh * G + vv % G) * HD;
+        if (col_ok)
+          *reinterpret_cast<uint2*>(dst + 4 * c4) =
+              make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+      } else {
+        if (col_ok) *reinterpret_cast<float4*>(a.part_o + qv * HD + 4 * c4) = acc;
+        if (lane == 0) *reinterpret_cast<float2*>(a.part_ml + qv * 2) = make_float2(M, lsum);
+      }
+    };
+    // a warp takes its rows four at a time (rr, rr + 8, rr + 16, rr + 24), all
+    // four rows' loads in flight before their stores
+    constexpr int RB = 4;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sp.S == 1) {
+      for (int r0 = sw; r0 < rows; r0 += 8 * RB) {
+        float4 acc[RB];
+        float2 ml[RB];
 #pragma unroll
-          for (int c = 0; c < HO; c += 4)
-            *reinterpret_cast<float4*>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-          if (half == 0) {
-            a.part_ml[qi * 2 + 0] = mrow;
-            a.part_ml[qi * 2 + 1] = lrow;
+        for (int u = 0; u < RB; ++u) {
+          const int rr = r0 + 8 * u;
+          acc[u] = rr < rows && col_ok ? *reinterpret_cast<const float4*>(xs + rr * XLD + 4 * c4) : zero4;
+          ml[u] = rr < rows ? *reinterpret_cast<const float2*>(xml + 2 * rr) : make_float2(0.f, 1.f);
+        }
+#pragma unroll
+        for (int u = 0; u < RB; ++u)
+          if (r0 + 8 * u < rows) write_final(r0 + 8 * u, acc[u], ml[u].x, ml[u].y);
+      }
+    } else {
+      // publish this split's partial state in slot 1 + s
+      const size_t TQ = (size_t)a.T * a.nq;
+      for (int r0 = sw; r0 < rows; r0 += 8 * RB) {
+        float4 val[RB];
+        float2 ml[RB];
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+          const int rr = r0 + 8 * u;
+          val[u] = rr < rows && col_ok ? *reinterpret_cast<const float4*>(xs + rr * XLD + 4 * c4) : zero4;
+          ml[u] = rr < rows ? *reinterpret_cast<const float2*>(xml + 2 * rr) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+          const int rr = r0 + 8 * u;
+          if (rr < rows) {
+            const size_t qv = (1 + s) * TQ + vec_index(rr);
+            if (col_ok) *reinterpret_cast<float4*>(a.part_o + qv * HD + 4 * c4) = val[u];
+            if (lane == 0) *reinterpret_cast<float2*>(a.part_ml + qv * 2) = ml[u];
           }
         }
       }
-    } else {
-      // rows [rank * per, (rank + 1) * per) of the tile are merged by `rank`
+      __threadfence();
+      // every split of the tile has published once the cluster has met
+      tc::cluster_sync_all();
+      // merge rows [s per, (s + 1) per): this split's own state from shared memory, the others' through L2
       const int per = (kTcQ + sp.S - 1) / sp.S;
-      // (the exchange area covers Q and the ring: wait until every split is past its loop)
-      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-      const int owner = row / per;
-      const uint32_t dst =
-          tc::map_to_rank(smem_addr(xbuf + ((size_t)s * per + (row - owner * per)) * Lay::XLD), (uint32_t)owner);
+      const int m_hi = min(rows, (s + 1) * per);
+      for (int r0 = s * per + sw; r0 < m_hi; r0 += 8 * RB) {
+        size_t qv[RB];
+        float2 ml[RB][kTcMaxSplits];
+        float4 part[RB][kTcMaxSplits];
 #pragma unroll
-      for (int c = 0; c < HO; c += 4)
-        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (half * HO + c) * 4), "f"(o[c]),
-                     "f"(o[c + 1]), "f"(o[c + 2]), "f"(o[c + 3])
-                     : "memory");
-      if (half == 0)
-        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(dst + HD * 4), "f"(mrow), "f"(lrow) : "memory");
-    }
-  }
-  if (sp.S > 1) {
-    if (warp < 2)  // the producer and MMA warps take part in the cluster barriers too
-      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    // merge: one warp per row (all warps), split weights formed once per row
-    const int rows = min((kTcQ + sp.S - 1) / sp.S, kTcQ - s * ((kTcQ + sp.S - 1) / sp.S));
-    const int per = (kTcQ + sp.S - 1) / sp.S;
-    for (int rl = warp; rl < rows; rl += kTcThreads / 32) {
-      const int v = q0 + s * per + rl;
-      if (v >= nqv) break;
-      float mt[kMaxSplits], w[kMaxSplits];
-      float M = -INFINITY;
+        for (int u = 0; u < RB; ++u) {
+          const int rr = r0 + 8 * u;
+          qv[u] = rr < m_hi ? vec_index(rr) : 0;
 #pragma unroll
-      for (int t = 0; t < kMaxSplits; ++t) {
-        mt[t] = t < sp.S ? xbuf[((size_t)t * per + rl) * Lay::XLD + HD] : -INFINITY;
-        M = fmaxf(M, mt[t]);
-      }
-      float lsum = 0.f;
-#pragma unroll
-      for (int t = 0; t < kMaxSplits; ++t) {
-        w[t] = t < sp.S ? exp2f(mt[t] - M) : 0.f;
-        if (t < sp.S) lsum += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + HD + 1];
-      }
-      if constexpr (kFused) {
-        const float inv = 1.f / lsum;
-        bf16* dst = reinterpret_cast<bf16*>(a.attn) + (size_t)(xr * a.L + v / G) * a.ld_attn + (kvh * G + v % G) * HD;
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          const int dd = lane + 32 * c;
-          float acc = 0.f;
-#pragma unroll
-          for (int t = 0; t < kMaxSplits; ++t)
-            if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + dd];
-          dst[dd] = __float2bfloat16_rn(acc * inv);
+          for (int t = 0; t < kTcMaxSplits; ++t) {
+            if (rr >= m_hi || t >= sp.S) {
+              ml[u][t] = make_float2(-INFINITY, 0.f);
+              part[u][t] = zero4;
+            } else if (t == s) {
+              ml[u][t] = *reinterpret_cast<const float2*>(xml + 2 * rr);
+              part[u][t] = col_ok ? *reinterpret_cast<const float4*>(xs + rr * XLD + 4 * c4) : zero4;
+            } else {
+              const size_t q = (1 + t) * TQ + qv[u];
+              ml[u][t] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + q * 2));
+              part[u][t] = col_ok ? __ldcg(reinterpret_cast<const float4*>(a.part_o + q * HD + 4 * c4)) : zero4;
+            }
+          }
         }
-      } else {
-        const size_t qi = (size_t)(off_r + v / G) * a.nq + kvh * G + v % G;
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          const int dd = lane + 32 * c;
-          float acc = 0.f;
+        for (int u = 0; u < RB; ++u) {
+          const int rr = r0 + 8 * u;
+          if (rr >= m_hi) continue;
+          float M = -INFINITY;
 #pragma unroll
-          for (int t = 0; t < kMaxSplits; ++t)
-            if (t < sp.S) acc += w[t] * xbuf[((size_t)t * per + rl) * Lay::XLD + dd];
-          a.part_o[qi * HD + dd] = acc;
-        }
-        if (lane == 0) {
-          a.part_ml[qi * 2 + 0] = M;
-          a.part_ml[qi * 2 + 1] = lsum;
+          for (int t = 0; t < kTcMaxSplits; ++t) M = fmaxf(M, ml[u][t].x);
+          float lsum = 0.f;
+          float4 acc = zero4;
+#pragma unroll
+          for (int t = 0; t < kTcMaxSplits; ++t) {
+            if (t < sp.S) {
+              const float w = exp2f(ml[u][t].x - M);
+              lsum += w * ml[u][t].y;
+              acc.x += w * part[u][t].x;
+              acc.y += w * part[u][t].y;
+              acc.z += w * part[u][t].z;
+              acc.w += w * part[u][t].w;
+            }
+          }
+          write_final(rr, acc, M, lsum);
         }
       }
     }
   }
+  // the other warps meet the cluster too (the softmax warps did above)
+  if (sp.S > 1 && (warp < 2 || warp >= 10)) tc::cluster_sync_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
@@ -1060,7 +1136,7 @@ cudaError_t attention_tc(Launch& lc, const AttnArgs& a) {
                                          TcLayout<HD>::BYTES);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_prefix_tc<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               TcLayout<HD, 3>::BYTES_FUSED);
+                               TcLayout<HD>::BYTES_FUSED);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_block_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, BlkLayout<HD>::bytes(64));
     return e;
@@ -1081,10 +1157,10 @@ cudaError_t attention_tc(Launch& lc, const AttnArgs& a) {
     if (fused) {
       const int tiles = (a.L * G + kTcQ - 1) / kTcQ;
       const Splits sp = fused_splits(a.P, a.R * a.Bp * a.nkv * tiles, a.target_ctas);
-      dim3 grid(a.R * a.Bp * a.nkv, tiles, sp.S);
+      dim3 grid(sp.S, a.R * a.Bp * a.nkv, tiles);
       lc.before(SF_K_ATTN_PREFIX);
-      lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD, 3>::BYTES_FUSED, sp.S,
-                          attn_prefix_tc<HD, true>, tmK, tmV, a));
+      lc.check(launch_pdl_cluster(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES_FUSED, dim3(sp.S, 1, 1),
+                                  attn_prefix_tc<HD, true>, tmK, tmV, a));
       lc.after(SF_K_ATTN_PREFIX);
       return lc.err;
     }
@@ -1092,9 +1168,9 @@ cudaError_t attention_tc(Launch& lc, const AttnArgs& a) {
     lc.before(SF_K_ATTN_PREFIX);
     {
       const Splits sp = tc_splits(a.P, a.R * a.nkv, a.target_ctas);
-      dim3 grid(a.R * a.nkv, (a.Bp * a.L * G + kTcQ - 1) / kTcQ, sp.S);
-      lc.check(launch_pdl(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES, sp.S, attn_prefix_tc<HD, false>,
-                          tmK, tmV, a));
+      dim3 grid(sp.S, a.R * a.nkv, (a.Bp * a.L * G + kTcQ - 1) / kTcQ);
+      lc.check(launch_pdl_cluster(lc.st, grid, dim3(kTcThreads), (size_t)TcLayout<HD>::BYTES, dim3(sp.S, 1, 1),
+                                  attn_prefix_tc<HD, false>, tmK, tmV, a));
     }
     lc.after(SF_K_ATTN_PREFIX);
   }

@@ -118,8 +118,8 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename Kernel, typename... Args>
-cudaError_t launch_pdl(cudaStream_t st, dim3 grid, dim3 block, size_t smem, int cluster_z, Kernel kernel,
-                       Args... args) {
+cudaError_t launch_pdl_cluster(cudaStream_t st, dim3 grid, dim3 block, size_t smem, dim3 cluster, Kernel kernel,
+                               Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -129,16 +129,24 @@ cudaError_t launch_pdl(cudaStream_t st, dim3 grid, dim3 block, size_t smem, int 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   int n = 1;
-  if (cluster_z > 1) {
+  if (cluster.x * cluster.y * cluster.z > 1) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = (unsigned)cluster_z;
+    attr[1].val.clusterDim.x = cluster.x;
+    attr[1].val.clusterDim.y = cluster.y;
+    attr[1].val.clusterDim.z = cluster.z;
     n = 2;
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// clusters (if any) along z
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(cudaStream_t st, dim3 grid, dim3 block, size_t smem, int cluster_z, Kernel kernel,
+                       Args... args) {
+  return launch_pdl_cluster(st, grid, block, smem, dim3(1, 1, cluster_z > 1 ? (unsigned)cluster_z : 1u), kernel,
+                            args...);
 }
 
 }  // namespace sf
