@@ -89,7 +89,11 @@ def test_modes_agree_on_the_first_layer():
 @pytest.mark.parametrize("kw", [dict(), dict(n_requests=3, n_q_heads=7, n_kv_heads=1, prefix_len=200, n_drafts=4),
                                 dict(prefix_len=2100, head_dim=64, n_q_heads=8, n_kv_heads=2, block_len=20,
                                      n_drafts=5),
-                                dict(prefix_len=1000, n_drafts=2, block_len=64)])
+                                dict(prefix_len=1000, n_drafts=2, block_len=64),
+                                # 25 (request, KV head) groups and 2,048 keys: three splits a query
+                                # tile on 152 SMs, merged 43 / 43 / 42 rows by the cluster's CTAs
+                                dict(n_requests=5, n_q_heads=5, n_kv_heads=5, head_dim=64, prefix_len=2048,
+                                     block_len=8, n_drafts=2)])
 def test_bf16_split_kernels_teacher_forced(kw):
     """SF_ATTN_DIRECT_SPLIT: the prefix-partial + block kernels that long
     prefixes take, forced on the small shapes that otherwise run fused."""

@@ -118,6 +118,10 @@ BF16_CASES = {
     "tc_prefix_hd64_ragged": dict(head_dim=64, n_q_heads=8, n_kv_heads=2, block_len=20, prefix_len=2100,
                                   n_drafts=5),
     "tc_prefix_three_requests_gqa7": dict(n_requests=3, n_q_heads=7, n_kv_heads=1, prefix_len=2048, n_drafts=4),
+    # fused kernel with three splits of the prefix (50 CTAs a split on 152 SMs):
+    # each split merges 43, 43 and 42 of a query tile's rows
+    "fused_three_splits": dict(head_dim=64, n_q_heads=10, n_kv_heads=10, block_len=8, prefix_len=512,
+                               n_drafts=4),
 }
 
 
