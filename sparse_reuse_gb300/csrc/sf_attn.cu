@@ -760,18 +760,8 @@ __global__ void __launch_bounds__(kBlkQ) attn_block_tc(const AttnArgs a) {
     }
     cp_async_commit();
   }
-  if (a.P > 0) {
-    pdl_wait();
-    pdl_trigger();
-  }
-  // the prefix state of this thread's query (previous kernel)
   size_t qi = 0;
-  float mp = 0.f, lp = 0.f;
   if (live) qi = (size_t)slot[vn] * a.nq + kvh * G + v % G;
-  if (a.P > 0 && live) {
-    mp = a.part_ml[qi * 2];
-    lp = a.part_ml[qi * 2 + 1];
-  }
   cp_async_wait<0>();
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
@@ -829,6 +819,19 @@ __global__ void __launch_bounds__(kBlkQ) attn_block_tc(const AttnArgs a) {
       tc::mma_bf16(tmem, dp, dv, idesc, kk > 0 ? 1u : 0u);
     }
     tc::mma_commit(&bar[1]);
+  }
+  // Everything above reads only the projected rows and the gate's slots
+  // (complete when this grid starts); the prefix kernel's partial state is
+  // read from here on.  A CTA that starts while the prefix kernel still runs
+  // has its block part done by the time the partial is ready.
+  float mp = 0.f, lp = 0.f;
+  if (a.P > 0) {
+    pdl_wait();
+    pdl_trigger();
+    if (live) {
+      mp = a.part_ml[qi * 2];
+      lp = a.part_ml[qi * 2 + 1];
+    }
   }
   // merge weights of the block part and the prefix partial
   float wb = 1.f, wp = 0.f, l = lb;
