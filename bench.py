@@ -522,9 +522,17 @@ def head_bench(args, dev, cfg):
     head.close()
     ctx.close()
     wb = (2 if cfg.dtype == "bf16" else 4) * cfg.d_model * synth.HEAD_VOCAB
+    # logits of every row: 2 rows d vocab FLOPs; the head is bound by the larger
+    # of its weight bytes at HBM bandwidth and its FLOPs at the bf16 peak
+    fl = 2.0 * cfg.rows * cfg.d_model * synth.HEAD_VOCAB
+    pk = peaks()
+    t_hbm, t_tensor = wb / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12)
     line = {"head": True, "config": workload_desc(cfg), "vocab": synth.HEAD_VOCAB, "delta": cfg.delta,
-            "ms_pass_plus_head": both, "ms_head": alone, "head_weight_bytes": wb,
-            "head_gbs": wb / (alone * 1e-3) / 1e9, "head_frac_hbm": wb / (alone * 1e-3) / 1e9 / peaks()["hbm_gbs"],
+            "ms_pass_plus_head": both, "ms_head": alone, "head_weight_bytes": wb, "head_flops": fl,
+            "head_bound": "tensor" if t_tensor > t_hbm else "hbm",
+            "head_frac_roofline": max(t_hbm, t_tensor) / (alone * 1e-3),
+            "head_tflops": fl / (alone * 1e-3) / 1e12, "head_frac_tensor": fl / (alone * 1e-3) / 1e12 / pk["bf16_tflops"],
+            "head_gbs": wb / (alone * 1e-3) / 1e9, "head_frac_hbm": wb / (alone * 1e-3) / 1e9 / pk["hbm_gbs"],
             "accepted_drafts": int(acc[:, 1:].sum().item()), "drafts": cfg.n_requests * cfg.n_drafts,
             "chosen": chosen.cpu().numpy().tolist()}
     print(json.dumps(line), flush=True)
