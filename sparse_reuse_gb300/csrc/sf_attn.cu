@@ -117,8 +117,6 @@ constexpr int kTcPVWarp = 11;
 constexpr int kTcMinKeysPerSplit = 512;
 constexpr int kTcMaxSplits = 4;
 static_assert(1 + kTcMaxSplits <= kMaxSplits, "split slots of the partial buffers");
-// Prefixes of at least this many keys take the tcgen05 kernel.
-constexpr int kTcMinPrefix = 1;
 constexpr float kTcRescaleLog2 = 8.f;
 
 // Few long splits: the fixed cost of a CTA (TMEM, barriers, the first scores,
@@ -632,7 +630,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_prefix_tc(const __grid_con
     }
   }
   // the other warps meet the cluster too (the softmax warps did above)
-  if (sp.S > 1 && (warp < 2 || warp >= 10)) tc::cluster_sync_all();
+  if (sp.S > 1 && (warp < 2 || warp == kTcVWarp || warp == kTcPVWarp)) tc::cluster_sync_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
