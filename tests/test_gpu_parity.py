@@ -137,6 +137,25 @@ def test_bf16_variants_teacher_forced(name):
         check_teacher_forced(cfg, wl, gpu, delta, range(cfg.n_layers))
 
 
+def test_bf16_random_norm_gains_teacher_forced():
+    """RMSNorm gains away from 1 (the synthetic weights use unit gains): the
+    attention gain goes through the gate's normalised rows, the FFN gain
+    through the O epilogue's bf16(h * g2) rows, with the row scale applied in
+    the gate/up epilogue."""
+    import torch
+    cfg = synth.small_config(n_layers=3, d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=128, d_ffn=320,
+                             dtype="bf16", block_len=32, prefix_len=96, n_drafts=4)
+    wl = _wl(cfg, seed=9)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(2024)
+    for W in wl.weights:
+        for key in ("attn_norm", "ffn_norm"):
+            W[key] = (0.5 + torch.rand(cfg.d_model, generator=g)).to(W[key].device, W[key].dtype)
+    for delta in (0.0, 0.1):
+        gpu = run_gpu(cfg, wl, delta)
+        check_teacher_forced(cfg, wl, gpu, delta, range(cfg.n_layers))
+
+
 def test_1p5b_all_layers_teacher_forced():
     cfg = synth.CONFIGS["1.5b"]
     wl = _wl(cfg)
