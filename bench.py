@@ -96,7 +96,7 @@ NCU_TRAFFIC = {
     ("14b", "gemm_down"): 151.71e6,
     ("14b", "gemm_o"): 91.63e6,
     ("14b", "gemm_qkv"): 77.29e6,
-    ("14b", "attn_prefix"): 71.17e6,
+    ("14b", "attn_prefix"): 71.26e6,
     ("14b", "attn_block"): 7.01e6,
 }
 
